@@ -1,0 +1,215 @@
+/*
+ * ROCmFP4 CPU oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, fp64 statement of what the ROCmFP4 block-quantised weight
+ * product computes.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load this file's library; the product
+ * path never does.  It shares no code, header, table or helper with the CUDA
+ * library: everything below is written out again from the format's
+ * definition.
+ *
+ * Source of the definitions: "Feasibility Report: Porting ROCmFP4 to Atlas",
+ * section "What is ROCmFP4?", subsections "Block Layout", "Codebook10 Value
+ * Table" and "Scale Format".
+ *
+ * Readings taken where that text is silent (each one is also pinned by the
+ * CPU tests in tests/test_oracle.py):
+ *   R1  nibble order inside qs[16]: byte j holds weight j in its low nibble
+ *       and weight j+16 in its high nibble (the ggml Q4_0 order the type
+ *       names Q4_0_ROCMFP4 / Q4_0_ROCMFP4_FAST point to).  Half 0 of a block
+ *       is therefore the 16 low nibbles, half 1 the 16 high nibbles.
+ *   R2  "decoded to half-scale values": the multiplier of a scale byte is
+ *       one half of its unsigned-E4M3 value.
+ *   R3  exponent field 0 decodes as an E4M3 subnormal, (M/8) * 2^-6.
+ *   R4  a scale byte is finite iff it is below 0x7F: bit 7 set (no sign in
+ *       an unsigned format) and 0x7F (exponent 15, mantissa 7) are rejected.
+ *   R5  code 8 ("-0" in the table) is the value +0.
+ *   R6  a row is K/32 blocks stored back to back, rows back to back, no
+ *       padding; K must be a multiple of 32.
+ * Parity with files written by the original implementation (R1, R2) is
+ * parity unpinned: no such file or printed example exists to compare with.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Codebook10, as printed in the "Codebook10 Value Table" subsection. */
+static const int8_t oracle_codebook10[16] = {
+    0, 1, 2, 3, 4, 6, 8, 10,
+    0, -1, -2, -3, -4, -6, -8, -10,
+};
+
+/* Block layout ("Block Layout" subsection): qs[16] followed by two scale
+ * bytes (dual-scale, 18 B) or one (fast single-scale, 17 B). */
+enum { ORACLE_DUAL = 0, ORACLE_FAST = 1 };
+enum { ORACLE_ACT_F16 = 0, ORACLE_ACT_BF16 = 1 };
+
+int oracle_block_bytes(int variant) {
+  if (variant == ORACLE_DUAL) return 18;
+  if (variant == ORACLE_FAST) return 17;
+  return -1;
+}
+
+int oracle_codebook(int q) { return oracle_codebook10[q & 15]; }
+
+/* Finite unsigned-E4M3 scale byte?  ("Scale Format": row validation rejects
+ * non-finite scale bytes; reading R4.) */
+int oracle_scale_is_valid(unsigned s) { return s < 0x7Fu; }
+
+/* Unsigned E4M3 value of a scale byte: 4 exponent bits (bias 7) above 3
+ * mantissa bits; exponent 0 is subnormal (reading R3). */
+double oracle_ue4m3_value(unsigned s) {
+  unsigned e = (s >> 3) & 0xFu;
+  unsigned m = s & 7u;
+  if (e == 0) return ldexp((double)m / 8.0, -6);
+  return ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+}
+
+/* Half-scale multiplier of a scale byte (reading R2). */
+double oracle_halfscale(unsigned s) { return 0.5 * oracle_ue4m3_value(s); }
+
+/* Nibble i (0..31) of a block's qs[16] (reading R1). */
+static unsigned oracle_nibble(const uint8_t *qs, int i) {
+  unsigned byte = qs[i % 16];
+  return (i < 16) ? (byte & 0xFu) : (byte >> 4);
+}
+
+/* Decode one block into its 32 weights: w_i = Codebook10[q_i] * hs(scale of
+ * the half that weight i belongs to). */
+void oracle_decode_block(const uint8_t *blk, int variant, double w[32]) {
+  const uint8_t *qs = blk;
+  for (int i = 0; i < 32; ++i) {
+    unsigned s = (variant == ORACLE_DUAL) ? blk[16 + i / 16] : blk[16];
+    double c = (double)oracle_codebook10[oracle_nibble(qs, i)];
+    w[i] = c * oracle_halfscale(s);
+    if (w[i] == 0.0) w[i] = 0.0; /* reading R5: no negative zero */
+  }
+}
+
+/* IEEE binary16 bits -> double (exact). */
+static double oracle_f16_value(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int m = h & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = (m == 0) ? INFINITY : NAN;
+  else v = ldexp((double)(1024 + m), e - 25);
+  return sign ? -v : v;
+}
+
+/* bfloat16 bits (the upper half of an IEEE binary32) -> double (exact). */
+static double oracle_bf16_value(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xFF;
+  int m = h & 0x7F;
+  double v;
+  if (e == 0) v = ldexp((double)m, -133);
+  else if (e == 255) v = (m == 0) ? INFINITY : NAN;
+  else v = ldexp((double)(128 + m), e - 134);
+  return sign ? -v : v;
+}
+
+double oracle_act_value(uint16_t bits, int act) {
+  return act == ORACLE_ACT_BF16 ? oracle_bf16_value(bits) : oracle_f16_value(bits);
+}
+
+static int oracle_check_shape(int64_t N, int64_t K, int variant) {
+  if (N < 0 || K < 0 || K % 32 != 0) return -1;
+  if (oracle_block_bytes(variant) < 0) return -1;
+  return 0;
+}
+
+/* Dense weights: out[n*K + k] = w[n][k] (row-major, fp64). */
+int oracle_dequant(const uint8_t *W, int64_t N, int64_t K, int variant, double *out) {
+  if (oracle_check_shape(N, K, variant)) return -1;
+  const int64_t bb = oracle_block_bytes(variant);
+  const int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b)
+      oracle_decode_block(W + (n * nb + b) * bb, variant, out + n * K + b * 32);
+  return 0;
+}
+
+/* First block (row-major block index n*nb + b) holding a scale byte that is
+ * not finite, or -1 when every scale byte is finite. */
+int64_t oracle_validate(const uint8_t *W, int64_t N, int64_t K, int variant) {
+  if (oracle_check_shape(N, K, variant)) return -2;
+  const int64_t bb = oracle_block_bytes(variant);
+  const int64_t nblk = N * (K / 32);
+  const int nscale = (variant == ORACLE_DUAL) ? 2 : 1;
+  for (int64_t i = 0; i < nblk; ++i)
+    for (int j = 0; j < nscale; ++j)
+      if (!oracle_scale_is_valid(W[i * bb + 16 + j])) return i;
+  return -1;
+}
+
+/* Y[m][n] = sum_k w[n][k] * x[m][k], summed in fp64 in increasing k.
+ * X holds M rows of K activation bit patterns (fp16 or bf16); Y is M x N.
+ * Rows n are split over nthreads POSIX threads; each output is summed by one
+ * thread in plain order, so the result does not depend on nthreads. */
+typedef struct {
+  const uint8_t *W;
+  const uint16_t *X;
+  double *Y;
+  int64_t M, N, K, n0, n1;
+  int variant, act;
+  int status;
+} oracle_gemm_job;
+
+static void *oracle_gemm_worker(void *arg) {
+  oracle_gemm_job *j = (oracle_gemm_job *)arg;
+  const int64_t K = j->K;
+  double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  double *x = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  if (!w || !x) { j->status = -3; free(w); free(x); return NULL; }
+  for (int64_t n = j->n0; n < j->n1; ++n) {
+    oracle_dequant(j->W + n * (K / 32) * oracle_block_bytes(j->variant), 1, K, j->variant, w);
+    for (int64_t m = 0; m < j->M; ++m) {
+      const uint16_t *xr = j->X + m * K;
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        x[k] = oracle_act_value(xr[k], j->act);
+        acc += w[k] * x[k];
+      }
+      j->Y[m * j->N + n] = acc;
+    }
+  }
+  free(w);
+  free(x);
+  j->status = 0;
+  return NULL;
+}
+
+int oracle_gemm(const uint8_t *W, const uint16_t *X, int act, double *Y, int64_t M,
+                int64_t N, int64_t K, int variant, int nthreads) {
+  if (oracle_check_shape(N, K, variant) || M < 0) return -1;
+  if (act != ORACLE_ACT_F16 && act != ORACLE_ACT_BF16) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > N) nthreads = (int)(N > 0 ? N : 1);
+  oracle_gemm_job *jobs = (oracle_gemm_job *)calloc((size_t)nthreads, sizeof(*jobs));
+  pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(*tid));
+  if (!jobs || !tid) { free(jobs); free(tid); return -3; }
+  for (int t = 0; t < nthreads; ++t) {
+    oracle_gemm_job *j = &jobs[t];
+    j->W = W; j->X = X; j->Y = Y; j->M = M; j->N = N; j->K = K;
+    j->variant = variant; j->act = act; j->status = -4;
+    j->n0 = N * t / nthreads;
+    j->n1 = N * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, oracle_gemm_worker, &jobs[t]) != 0) break;
+    started = t;
+  }
+  oracle_gemm_worker(&jobs[0]);
+  for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+  for (int t = started + 1; t < nthreads; ++t) oracle_gemm_worker(&jobs[t]); /* not started */
+  int status = 0;
+  for (int t = 0; t < nthreads; ++t) if (jobs[t].status != 0) status = jobs[t].status;
+  free(jobs);
+  free(tid);
+  return status;
+}

@@ -1,0 +1,187 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each check compares the oracle with something it does not compute itself:
+values printed on the pages (tests/golden), hand-worked blocks, a library
+routine (torch's float8_e4m3fn and numpy's float16 decoders), or exact
+brute force on inputs whose sums are exact in fp64.  ``pin_failures(L)``
+returns the list of failed checks for an oracle library ``L`` (``None`` = the
+real oracle); the tests require it to be empty for the real oracle and
+non-empty for every deliberately broken copy.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from golden_io import lines
+
+DUAL, FAST = oracle.DUAL, oracle.FAST
+
+
+def golden_codebook():
+    rows = list(lines("codebook10.txt"))
+    table = [int(v) for v in rows[0].split()]
+    e2m1 = [float(v) for v in rows[1].split(":")[1].split()]
+    return table, e2m1
+
+
+def golden_layout():
+    out = {}
+    for ln in lines("block_layout.txt"):
+        name, wpb, qs, sc, bb, bpw = ln.split()
+        out[name] = (int(wpb), int(qs), int(sc), int(bb), float(bpw))
+    return out
+
+
+def golden_ue4m3():
+    out = []
+    for ln in lines("ue4m3_spot.txt"):
+        b, e, m, v, hs, fin = ln.split()
+        out.append((int(b, 16), int(e), int(m), float(v), float(hs), bool(int(fin))))
+    return out
+
+
+def golden_decoded_block():
+    rows = list(lines("decoded_block.txt"))
+    blk = np.array([int(v, 16) for v in rows[0].split()], dtype=np.uint8)
+    w = np.array([float(v) for v in rows[1].split()] + [float(v) for v in rows[2].split()])
+    return blk, w
+
+
+def golden_hand_blocks():
+    out = []
+    for ln in lines("hand_blocks.txt"):
+        name, var, qs, e0, e1, xa, xb, y, y_alt = ln.split()
+        out.append(dict(name=name, variant=DUAL if var == "dual" else FAST, qs=int(qs, 16),
+                        e0=int(e0, 16), e1=None if e1 == "-" else int(e1, 16),
+                        xa=float(xa), xb=float(xb), y=float(y), y_alt=float(y_alt)))
+    return out
+
+
+def f16_bits(values) -> np.ndarray:
+    return np.asarray(values, dtype=np.float16).view(np.uint16)
+
+
+def hand_block_bytes(case) -> np.ndarray:
+    blk = [case["qs"]] * 16 + [case["e0"]]
+    if case["variant"] == DUAL:
+        blk.append(case["e1"])
+    return np.array(blk, dtype=np.uint8)
+
+
+def torch_e4m3_values() -> np.ndarray:
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_failures(L=None) -> list[str]:
+    fails: list[str] = []
+
+    def check(name, ok):
+        if not ok:
+            fails.append(name)
+
+    for section in (_pin_tables, _pin_scales, _pin_blocks, _pin_activations, _pin_brute_force,
+                    _pin_validate):
+        try:
+            with np.errstate(invalid="ignore"):
+                section(check, L)
+        except Exception as exc:  # a broken oracle may also fail loudly
+            fails.append(f"{section.__name__}: {type(exc).__name__}: {exc}")
+    return fails
+
+
+def _pin_tables(check, L):
+    # 1. Codebook10 as printed; it is doubled E2M1 with 12 retuned to 10.
+    table, e2m1 = golden_codebook()
+    cb = [oracle.codebook(q, L) for q in range(16)]
+    check("codebook table", cb == table)
+    doubled = [2 * v for v in e2m1] + [-2 * v for v in e2m1]
+    check("codebook vs doubled e2m1", all(
+        (c == d) or (q % 8 == 7 and abs(d) == 12 and abs(c) == 10) for q, (c, d) in enumerate(zip(cb, doubled))))
+
+    # 2. Block sizes and bits per weight as printed.
+    lay = golden_layout()
+    for name, var in (("dual", DUAL), ("fast", FAST)):
+        wpb, qs, sc, bb, bpw = lay[name]
+        got = oracle.block_bytes(var, L)
+        check(f"block bytes {name}", got == bb == qs + sc)
+        check(f"bpw {name}", abs(got * 8 / wpb - bpw) < 1e-12)
+
+
+def _pin_scales(check, L):
+    # 3. Scale decode: E4M3 value of every finite code equals torch's
+    #    float8_e4m3fn decoder; spot values worked by hand; finiteness.
+    ref = torch_e4m3_values()
+    for s in range(0x7F):
+        check(f"ue4m3 {s:#04x} vs torch", oracle.ue4m3(s, L) == ref[s])
+        check(f"halfscale {s:#04x}", oracle.halfscale(s, L) == 0.5 * ref[s])
+    for s in range(256):
+        finite = s < 0x80 and np.isfinite(ref[s])
+        check(f"validity {s:#04x}", oracle.scale_is_valid(s, L) == finite)
+    for b, e, m, v, hs, fin in golden_ue4m3():
+        check(f"spot validity {b:#04x}", oracle.scale_is_valid(b, L) == fin)
+        if fin:
+            check(f"spot value {b:#04x}", oracle.ue4m3(b, L) == v and oracle.halfscale(b, L) == hs)
+
+
+def _pin_blocks(check, L):
+    # 4. A block decoded by hand, weight by weight (signs, both halves, code 8 -> +0).
+    blk, w_ref = golden_decoded_block()
+    w = oracle.decode_block(blk, DUAL, L)
+    check("decoded block", np.array_equal(w, w_ref) and not np.any(np.signbit(w[w == 0])))
+    wd = oracle.dequant(blk, 1, 32, DUAL, L)[0]
+    check("dequant = decode_block", np.array_equal(wd, w_ref))
+
+    # 5. Single-block products worked by hand.
+    for case in golden_hand_blocks():
+        x = f16_bits([case["xa"]] * 16 + [case["xb"]] * 16)
+        y = oracle.gemv(hand_block_bytes(case), x, 1, 32, case["variant"], L=L)[0]
+        check(f"hand block {case['name']}", y == case["y"])
+
+
+def _pin_activations(check, L):
+    # 6. Activation decoders: every 7th fp16 / bf16 bit pattern vs numpy.
+    bits = np.arange(65536, dtype=np.uint16)
+    f16 = bits.view(np.float16).astype(np.float64)
+    f16_o = np.array([oracle.act_value(b, oracle.ACT_F16, L) for b in range(0, 65536, 7)])
+    check("fp16 decode", np.array_equal(f16_o, f16[::7], equal_nan=True))
+    bf16 = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    bf16_o = np.array([oracle.act_value(b, oracle.ACT_BF16, L) for b in range(0, 65536, 7)])
+    check("bf16 decode", np.array_equal(bf16_o, bf16[::7], equal_nan=True))
+
+
+def _pin_brute_force(check, L):
+    # 7. Brute force: x and weights chosen so every sum is exact in fp64, so
+    #    the oracle must equal a dense numpy matmul of the dequantised matrix
+    #    to the last bit (M > 1 and N > 1 catch swapped or transposed indices).
+    rng = np.random.default_rng(7)
+    for var in (DUAL, FAST):
+        N, K, M = 5, 96, 3
+        W = synth.weights(N, K, var, seed=3, stream=11)
+        X = f16_bits(rng.integers(-8, 9, size=(M, K)).astype(np.float64) * 0.25)
+        dense = oracle.dequant(W, N, K, var, L)
+        Xf = X.view(np.float16).astype(np.float64)
+        Y = oracle.gemm(W, X, N, K, var, nthreads=2, L=L)
+        check(f"brute force exact {var}", np.array_equal(Y, Xf @ dense.T))
+        # dense rows agree with block-by-block decoding
+        rb = oracle.row_bytes(K, var, L)
+        bb = oracle.block_bytes(var, L)
+        blocks = np.concatenate([oracle.decode_block(W[n, b * bb:(b + 1) * bb], var, L)
+                                 for n in range(N) for b in range(rb // bb)])
+        check(f"dequant rows {var}", np.array_equal(blocks.reshape(N, K), dense))
+
+
+def _pin_validate(check, L):
+    # 8. Validation finds a planted non-finite scale byte (second half too).
+    for var, off in ((DUAL, 16), (DUAL, 17), (FAST, 16)):
+        N, K = 3, 64
+        W = synth.weights(N, K, var, seed=0, stream=2).copy()
+        bb = oracle.block_bytes(var, L)
+        check(f"validate clean {var}", oracle.validate(W, N, K, var, L) == -1)
+        flat = W.reshape(-1)
+        flat[4 * bb + off] = 0x7F
+        flat[5 * bb + 16] = 0x80
+        check(f"validate planted {var}/{off}", oracle.validate(W, N, K, var, L) == 4)
