@@ -1,0 +1,179 @@
+"""Python binding of the GB300 ROCmFP4 library (``include/rocmfp4.h``).
+
+Argument marshalling only: every step of dequantisation and of the products
+runs in the CUDA kernels of ``_build/librocmfp4.so``.  There is no CPU
+fallback: if the library is missing or no GPU is present, calls raise.
+
+Entry points (names as in the C ABI, without the ``rocmfp4_`` prefix):
+``gemv``, ``gemm``, ``dequant``, ``validate``, ``block_bytes``, ``row_bytes``.
+Tensors are torch CUDA tensors; packed weights are ``uint8`` tensors holding
+``N * row_bytes(K, variant)`` bytes; activations are ``float16`` or
+``bfloat16``; outputs are ``float32``.  Calls are asynchronous on torch's
+current CUDA stream unless a stream is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+DUAL, FAST = 0, 1
+ACT_F16, ACT_BF16 = 0, 1
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPORTED",
+          3: "ROCMFP4_ERR_INVALID_SCALE", 4: "ROCMFP4_ERR_CUDA"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
+EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
+           "rocmfp4_gemm_ex", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
+
+_lib = None
+
+
+class RocmFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str, message: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} {message}".strip())
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (build it first with ``build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"ROCmFP4 CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    L = ctypes.CDLL(path)
+    vp, i64, c_int, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+    sig = {
+        "rocmfp4_block_bytes": ([c_int], ctypes.c_size_t),
+        "rocmfp4_row_bytes": ([i64, c_int], ctypes.c_size_t),
+        "rocmfp4_gemv": ([vp, vp, vp, i64, i64, c_int], c_int),
+        "rocmfp4_gemv_ex": ([vp, vp, vp, i64, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_gemm": ([vp, vp, vp, i64, i64, i64, c_int], c_int),
+        "rocmfp4_gemm_ex": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
+        "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
+        "rocmfp4_device_error_bits": ([vp], u32),
+        "rocmfp4_status_string": ([c_int], ctypes.c_char_p),
+        "rocmfp4_last_error": ([], ctypes.c_char_p),
+        "rocmfp4_launch_count": ([], ctypes.c_uint64),
+        "rocmfp4_shutdown": ([], None),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        msg = load().rocmfp4_last_error().decode(errors="replace")
+        raise RocmFP4Error(status, where, msg)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _act_of(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ACT_F16
+    if t.dtype == torch.bfloat16:
+        return ACT_BF16
+    raise TypeError(f"activations must be float16 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def block_bytes(variant: int) -> int:
+    return int(load().rocmfp4_block_bytes(variant))
+
+
+def row_bytes(K: int, variant: int) -> int:
+    return int(load().rocmfp4_row_bytes(K, variant))
+
+
+def _check_w(W, N: int, K: int, variant: int):
+    torch = _torch()
+    if W.dtype != torch.uint8 or not W.is_cuda or not W.is_contiguous():
+        raise TypeError("W must be a contiguous uint8 CUDA tensor")
+    if W.numel() < N * row_bytes(K, variant):
+        raise ValueError("W holds fewer than N * row_bytes bytes")
+
+
+def gemm(W, X, N: int, K: int, variant: int = DUAL, Y=None, stream=None):
+    """Y[M, N] = X[M, K] . W^T in fp32 (X fp16 or bf16, on the GPU)."""
+    torch = _torch()
+    _check_w(W, N, K, variant)
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    if not X.is_cuda or not X.is_contiguous() or X.shape[1] != K:
+        raise ValueError("X must be a contiguous [M, K] CUDA tensor")
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    elif Y.dtype != torch.float32 or not Y.is_contiguous() or Y.numel() < M * N:
+        raise ValueError("Y must be a contiguous float32 tensor with M*N elements")
+    _check(load().rocmfp4_gemm_ex(_ptr(W), _ptr(X), _ptr(Y), M, N, K, variant, _act_of(X), _stream(stream)),
+           "rocmfp4_gemm_ex")
+    return Y
+
+
+def gemv(W, x, N: int, K: int, variant: int = DUAL, y=None, stream=None):
+    """y[N] = W . x in fp32 (x fp16 or bf16, length K)."""
+    torch = _torch()
+    _check_w(W, N, K, variant)
+    if not x.is_cuda or not x.is_contiguous() or x.numel() != K:
+        raise ValueError("x must be a contiguous CUDA tensor of K elements")
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    _check(load().rocmfp4_gemv_ex(_ptr(W), _ptr(x), _ptr(y), N, K, variant, _act_of(x), _stream(stream)),
+           "rocmfp4_gemv_ex")
+    return y
+
+
+def dequant(W, N: int, K: int, variant: int = DUAL, out_dtype=None, out=None, stream=None):
+    """Dense [N, K] weights (float32 by default, or bfloat16 / float16), exact."""
+    torch = _torch()
+    _check_w(W, N, K, variant)
+    dt = out_dtype or (out.dtype if out is not None else torch.float32)
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16, torch.float16: OUT_F16}[dt]
+    if out is None:
+        out = torch.empty((N, K), dtype=dt, device=W.device)
+    _check(load().rocmfp4_dequant(_ptr(W), _ptr(out), code, N, K, variant, _stream(stream)), "rocmfp4_dequant")
+    return out
+
+
+def validate(W, N: int, K: int, variant: int = DUAL, stream=None) -> int:
+    """-1 if every scale byte is finite, else the index of the first bad block."""
+    _check_w(W, N, K, variant)
+    first = ctypes.c_int64(-1)
+    st = load().rocmfp4_validate(_ptr(W), N, K, variant, ctypes.byref(first), _stream(stream))
+    if st not in (0, 3):
+        _check(st, "rocmfp4_validate")
+    return int(first.value)
+
+
+def device_error_bits(stream=None) -> int:
+    return int(load().rocmfp4_device_error_bits(_stream(stream)))
+
+
+def launch_count() -> int:
+    return int(load().rocmfp4_launch_count())

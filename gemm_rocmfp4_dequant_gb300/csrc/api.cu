@@ -1,0 +1,276 @@
+// C ABI of the ROCmFP4 library (declared in include/rocmfp4.h): host-side
+// argument checks, per-device state, and kernel dispatch.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/rocmfp4.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace rocmfp4;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int occ[2][2] = {{0, 0}, {0, 0}};  // stream kernel CTAs per SM [variant][act]
+  int64_t wmax = 0;                  // workspace capacity in warps
+  float* ws = nullptr;               // 2 * wmax records of 128 floats
+  uint32_t* cnt = nullptr;           // wmax split counters
+  uint32_t* err = nullptr;           // kernel error bits
+  unsigned long long* vfirst = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};
+thread_local std::string t_last_error;
+
+rocmfp4_status fail(rocmfp4_status st, const std::string& msg) {
+  t_last_error = msg;
+  return st;
+}
+
+rocmfp4_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ROCMFP4_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_variant(int v) { return v == ROCMFP4_DUAL || v == ROCMFP4_FAST; }
+bool valid_act(int a) { return a == ROCMFP4_ACT_F16 || a == ROCMFP4_ACT_BF16; }
+
+int64_t block_bytes_of(int v) { return v == ROCMFP4_DUAL ? 18 : 17; }
+
+// Per-device set-up on first use: SM count, kernel attributes, occupancy and
+// the workspace of the split-tile reduction.
+rocmfp4_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ROCMFP4_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    int best = 1;
+    for (int v = 0; v < 2; ++v)
+      for (int a = 0; a < 2; ++a) {
+        if ((e = stream_prepare(v, a)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        if ((e = stream_occupancy(v, a, &d.occ[v][a])) != cudaSuccess) return cuda_fail(e, "occupancy");
+        if (d.occ[v][a] < 1) return fail(ROCMFP4_ERR_UNSUPPORTED, "streaming kernel does not fit on this device");
+        best = d.occ[v][a] > best ? d.occ[v][a] : best;
+      }
+    d.wmax = (int64_t)d.sms * best * kStreamWarpsPerCta;
+    if ((e = cudaMalloc(&d.ws, sizeof(float) * 128 * 2 * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.cnt, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.err, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.vfirst, sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(d.cnt, 0, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    if ((e = cudaMemset(d.err, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    d.ready = true;
+  }
+  *out = &d;
+  return ROCMFP4_OK;
+}
+
+rocmfp4_status check_shape(int64_t N, int64_t K, int variant) {
+  if (!valid_variant(variant)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown variant");
+  if (N < 0 || K < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  if (K % 32 != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "K must be a multiple of 32");
+  return ROCMFP4_OK;
+}
+
+rocmfp4_status check_matrix(const void* W, int64_t N, int64_t K, int variant) {
+  rocmfp4_status st = check_shape(N, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  if (N > 0 && K > 0 && W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
+  return ROCMFP4_OK;
+}
+
+rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K, int variant,
+                       int act, cudaStream_t s) {
+  rocmfp4_status st = check_shape(N, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  if (!valid_act(act)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown activation type");
+  if (M < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  if (M == 0 || N == 0) return ROCMFP4_OK;
+  if (Y == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "Y is NULL");
+  if (K > 0 && W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, sizeof(float) * M * N, s);
+    return e == cudaSuccess ? ROCMFP4_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+  if (X == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "X is NULL");
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ROCMFP4_OK) return st;
+
+  const int64_t row_bytes = K / 32 * block_bytes_of(variant);
+  const int64_t ku = stream_weights_per_unit(variant);
+  const bool stream_ok = K % ku == 0 && aligned16(W) && aligned16(X);
+  const uint16_t* Xh = static_cast<const uint16_t*>(X);
+  if (!stream_ok) {
+    GenericArgs a{static_cast<const uint8_t*>(W), Xh, Y, N, K, row_bytes, M};
+    cudaError_t e = launch_gemm_generic(variant, act, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "generic kernel launch");
+    g_launches.fetch_add(1);
+    return ROCMFP4_OK;
+  }
+  const int64_t nspans = K / ku;
+  const int64_t units = (N + 15) / 16 * nspans;
+  const int64_t cap = (int64_t)d->sms * d->occ[variant][act] * kStreamWarpsPerCta;
+  const int64_t wact = units < cap ? units : cap;
+  const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
+  for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    GemvArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.X = Xh + m0 * K;
+    a.Y = Y + m0 * N;
+    a.N = N;
+    a.K = K;
+    a.row_bytes = row_bytes;
+    a.M = (int)(M - m0 < 8 ? M - m0 : 8);
+    a.nspans = nspans;
+    a.units = units;
+    a.wact = wact;
+    a.ws = d->ws;
+    a.cnt = d->cnt;
+    a.err = d->err;
+    cudaError_t e = launch_gemv_stream(variant, act, a, ctas, s);
+    if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
+    g_launches.fetch_add(1);
+  }
+  return ROCMFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rocmfp4_block_bytes(rocmfp4_variant variant) {
+  return valid_variant(variant) ? (size_t)block_bytes_of(variant) : 0;
+}
+
+size_t rocmfp4_row_bytes(int64_t K, rocmfp4_variant variant) {
+  if (!valid_variant(variant) || K < 0 || K % 32 != 0) return 0;
+  return (size_t)(K / 32 * block_bytes_of(variant));
+}
+
+rocmfp4_status rocmfp4_gemv(const void* W, const void* x, float* y, int64_t N, int64_t K,
+                            rocmfp4_variant variant) {
+  return product(W, x, y, 1, N, K, variant, ROCMFP4_ACT_F16, nullptr);
+}
+
+rocmfp4_status rocmfp4_gemv_ex(const void* W, const void* x, float* y, int64_t N, int64_t K,
+                               rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
+  return product(W, x, y, 1, N, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rocmfp4_status rocmfp4_gemm(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
+                            rocmfp4_variant variant) {
+  return product(W, X, Y, M, N, K, variant, ROCMFP4_ACT_BF16, nullptr);
+}
+
+rocmfp4_status rocmfp4_gemm_ex(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
+                               rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
+  return product(W, X, Y, M, N, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rocmfp4_status rocmfp4_dequant(const void* W, void* out, rocmfp4_out_dtype out_dtype, int64_t N, int64_t K,
+                               rocmfp4_variant variant, rocmfp4_stream_t stream) {
+  rocmfp4_status st = check_shape(N, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  if (out_dtype != ROCMFP4_OUT_F32 && out_dtype != ROCMFP4_OUT_BF16 && out_dtype != ROCMFP4_OUT_F16)
+    return fail(ROCMFP4_ERR_INVALID_ARG, "unknown output type");
+  const int64_t nblocks = N * (K / 32);
+  if (nblocks == 0) return ROCMFP4_OK;
+  if (W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
+  if (out == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "out is NULL");
+  cudaError_t e = launch_dequant(variant, out_dtype, static_cast<const uint8_t*>(W), out, nblocks,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+  g_launches.fetch_add(1);
+  return ROCMFP4_OK;
+}
+
+rocmfp4_status rocmfp4_validate(const void* W, int64_t N, int64_t K, rocmfp4_variant variant,
+                                int64_t* first_bad_block, rocmfp4_stream_t stream) {
+  if (first_bad_block) *first_bad_block = -1;
+  rocmfp4_status st = check_shape(N, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  const int64_t nblocks = N * (K / 32);
+  if (nblocks == 0) return ROCMFP4_OK;
+  if (W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ROCMFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long first = ~0ull;
+  cudaError_t e = cudaMemcpyAsync(d->vfirst, &first, sizeof(first), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  if ((e = launch_validate(variant, static_cast<const uint8_t*>(W), nblocks, d->vfirst, s)) != cudaSuccess)
+    return cuda_fail(e, "validate launch");
+  g_launches.fetch_add(1);
+  if ((e = cudaMemcpyAsync(&first, d->vfirst, sizeof(first), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpyAsync");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (first == ~0ull) return ROCMFP4_OK;
+  if (first_bad_block) *first_bad_block = (int64_t)first;
+  return ROCMFP4_ERR_INVALID_SCALE;
+}
+
+uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream) {
+  DeviceState* d = nullptr;
+  if (device_state(&d) != ROCMFP4_OK) return 0xFFFFFFFFu;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, d->err, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return 0xFFFFFFFFu;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return 0xFFFFFFFFu;
+  if (bits != 0) {
+    // A kernel gave up waiting: its split counters may be left set, so clear them.
+    cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
+    cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
+    cudaStreamSynchronize(s);
+  }
+  return bits;
+}
+
+const char* rocmfp4_status_string(rocmfp4_status status) {
+  switch (status) {
+    case ROCMFP4_OK: return "ROCMFP4_OK";
+    case ROCMFP4_ERR_INVALID_ARG: return "ROCMFP4_ERR_INVALID_ARG";
+    case ROCMFP4_ERR_UNSUPPORTED: return "ROCMFP4_ERR_UNSUPPORTED";
+    case ROCMFP4_ERR_INVALID_SCALE: return "ROCMFP4_ERR_INVALID_SCALE";
+    case ROCMFP4_ERR_CUDA: return "ROCMFP4_ERR_CUDA";
+  }
+  return "ROCMFP4_UNKNOWN_STATUS";
+}
+
+const char* rocmfp4_last_error(void) { return t_last_error.c_str(); }
+
+uint64_t rocmfp4_launch_count(void) { return g_launches.load(); }
+
+void rocmfp4_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (int dev = 0; dev < kMaxDevices; ++dev) {
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) continue;
+    cudaSetDevice(dev);
+    cudaDeviceSynchronize();
+    cudaFree(d.ws);
+    cudaFree(d.cnt);
+    cudaFree(d.err);
+    cudaFree(d.vfirst);
+    d = DeviceState{};
+  }
+  cudaSetDevice(cur);
+}
+
+}  // extern "C"

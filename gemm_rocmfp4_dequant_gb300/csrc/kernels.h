@@ -1,0 +1,48 @@
+// Host-side launch interface between api.cu and the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rocmfp4 {
+
+// Streaming product Y[M][N] = X[M][K] . W[N][K]^T for M <= 8.
+struct GemvArgs {
+  const uint8_t* W;      // N x row_bytes packed blocks
+  const uint16_t* X;     // M x K activations (fp16 or bf16 bits)
+  float* Y;              // M x N outputs
+  int64_t N, K, row_bytes;
+  int M;
+  int64_t nspans;        // K / weights-per-unit
+  int64_t units;         // ceil(N/16) * nspans
+  int64_t wact;          // active warps (<= units)
+  float* ws;             // 2 * wact records of 16 x 8 floats
+  uint32_t* cnt;         // wact counters, zero between calls
+  uint32_t* err;         // error bits
+};
+
+constexpr int kStreamWarpsPerCta = 4;
+int stream_weights_per_unit(int variant);   // 256 (dual) or 512 (single-scale)
+size_t stream_smem_bytes(int variant);
+cudaError_t stream_prepare(int variant, int act);  // sets the dynamic smem attribute
+cudaError_t stream_occupancy(int variant, int act, int* ctas_per_sm);
+cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s);
+
+// Any K % 32 == 0, any alignment: one warp per (row, column chunk).
+struct GenericArgs {
+  const uint8_t* W;
+  const uint16_t* X;
+  float* Y;
+  int64_t N, K, row_bytes;
+  int64_t M;
+};
+cudaError_t launch_gemm_generic(int variant, int act, const GenericArgs& a, cudaStream_t s);
+
+// Dequantisation to fp32 / bf16 / fp16 (out_dtype 0/1/2), flat over blocks.
+cudaError_t launch_dequant(int variant, int out_dtype, const uint8_t* W, void* out, int64_t nblocks,
+                           cudaStream_t s);
+
+// First block with a non-finite scale byte -> atomicMin into *first (init INT64_MAX).
+cudaError_t launch_validate(int variant, const uint8_t* W, int64_t nblocks, unsigned long long* first,
+                            cudaStream_t s);
+
+}  // namespace rocmfp4

@@ -1,0 +1,150 @@
+/*
+ * rocmfp4.h -- C ABI of the GB300 (sm_103a) ROCmFP4 library.
+ *
+ * ROCmFP4 is the 4-bit block format defined on the page "Feasibility Report:
+ * Porting ROCmFP4 to Atlas", section "What is ROCmFP4?":
+ *   - subsection "Block Layout": a block holds 32 weights as qs[16] (32 packed
+ *     4-bit codes) followed by e[2] (dual-scale, 18 bytes, one scale per
+ *     16-weight half, type Q4_0_ROCMFP4) or by e (single-scale "fast" block,
+ *     17 bytes, type Q4_0_ROCMFP4_FAST);
+ *   - subsection "Codebook10 Value Table": code q maps to
+ *     {0,1,2,3,4,6,8,10,0,-1,-2,-3,-4,-6,-8,-10}[q];
+ *   - subsection "Scale Format": scale bytes are finite unsigned E4M3 values
+ *     used as half-scales.
+ * This library reads them as follows (the same readings the test oracle
+ * takes):
+ *   - byte j of qs holds weight j in its low nibble and weight j+16 in its
+ *     high nibble; the first scale covers weights 0..15, the second 16..31;
+ *   - weight = Codebook10[q] * hs(e), hs(e) = one half of the unsigned E4M3
+ *     value of e (exponent bits 6..3 with bias 7, mantissa bits 2..0,
+ *     exponent 0 subnormal); code 8 is +0;
+ *   - a scale byte is finite iff it is below 0x7F;
+ *   - a matrix of N rows and K columns (K a multiple of 32) is N rows of K/32
+ *     blocks, rows and blocks back to back with no padding
+ *     (row_bytes = K/32 * block_bytes).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer to matrix, activation or output data is DEVICE memory
+ *     owned by the caller.  Calls do not allocate per call; a small per-device
+ *     workspace (split-reduction partials and counters) is allocated once, on
+ *     first use, and released by rocmfp4_shutdown().
+ *   - Calls are asynchronous on the given CUDA stream (NULL = legacy default
+ *     stream) except rocmfp4_validate, which waits for its own result.
+ *   - Arguments are checked on the host: a NULL pointer with a non-empty
+ *     shape, a negative size, K not a multiple of 32 or an unknown enum value
+ *     returns ROCMFP4_ERR_INVALID_ARG and launches nothing.  A failed launch
+ *     returns ROCMFP4_ERR_CUDA (rocmfp4_last_error() gives the CUDA message).
+ *   - Weights are assumed validated (rocmfp4_validate): outputs computed from
+ *     a non-finite scale byte are unspecified, but no access ever leaves the
+ *     caller's buffers.
+ *   - Outputs must not overlap inputs.  Results are bitwise identical from
+ *     run to run for the same shapes on the same device (fixed reduction
+ *     order, no floating-point atomics).
+ *   - Empty shapes (N == 0, M == 0 or K == 0) are valid; K == 0 writes zeros.
+ */
+#ifndef ROCMFP4_H_
+#define ROCMFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st *rocmfp4_stream_t;
+
+typedef enum {
+  ROCMFP4_DUAL = 0, /* 18-byte block, two half-scales (Q4_0_ROCMFP4)        */
+  ROCMFP4_FAST = 1  /* 17-byte block, one scale (Q4_0_ROCMFP4_FAST)          */
+} rocmfp4_variant;
+
+typedef enum {
+  ROCMFP4_ACT_F16 = 0, /* activations are IEEE binary16                     */
+  ROCMFP4_ACT_BF16 = 1 /* activations are bfloat16                          */
+} rocmfp4_act;
+
+typedef enum {
+  ROCMFP4_OUT_F32 = 0,
+  ROCMFP4_OUT_BF16 = 1,
+  ROCMFP4_OUT_F16 = 2
+} rocmfp4_out_dtype;
+
+typedef enum {
+  ROCMFP4_OK = 0,
+  ROCMFP4_ERR_INVALID_ARG = 1,   /* bad pointer, size or enum value          */
+  ROCMFP4_ERR_UNSUPPORTED = 2,   /* valid request this build cannot serve    */
+  ROCMFP4_ERR_INVALID_SCALE = 3, /* rocmfp4_validate found a non-finite scale */
+  ROCMFP4_ERR_CUDA = 4           /* a CUDA call failed                        */
+} rocmfp4_status;
+
+/* Bytes of one block: 18 (ROCMFP4_DUAL), 17 (ROCMFP4_FAST), 0 otherwise.
+ * ("Block Layout": 4.50 and 4.25 bits per weight.) */
+size_t rocmfp4_block_bytes(rocmfp4_variant variant);
+
+/* Bytes of one packed row of K weights (K/32 blocks); 0 on a bad argument. */
+size_t rocmfp4_row_bytes(int64_t K, rocmfp4_variant variant);
+
+/* Batch-1 decode product y = W . x.
+ *   W: N x K packed ROCmFP4 matrix (N * row_bytes bytes).
+ *   x: K activations, fp16.        y: N fp32 outputs, overwritten.
+ * Same as rocmfp4_gemv_ex(..., ROCMFP4_ACT_F16, NULL). */
+rocmfp4_status rocmfp4_gemv(const void *W, const void *x, float *y, int64_t N, int64_t K,
+                            rocmfp4_variant variant);
+
+/* y = W . x with the activation type and stream given.  x is K elements of
+ * type act; y is N fp32, overwritten.  Accumulation is fp32. */
+rocmfp4_status rocmfp4_gemv_ex(const void *W, const void *x, float *y, int64_t N, int64_t K,
+                               rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream);
+
+/* Y = X . W^T: X is M x K activations (row-major), W is N x K packed,
+ * Y is M x N fp32 (row-major), overwritten.  Plain form: X is bf16, default
+ * stream.  M <= 8 runs the small-batch streaming kernel (each weight byte read
+ * once for all M vectors); larger M runs the tensor-core prefill kernel. */
+rocmfp4_status rocmfp4_gemm(const void *W, const void *X, float *Y, int64_t M, int64_t N, int64_t K,
+                            rocmfp4_variant variant);
+
+rocmfp4_status rocmfp4_gemm_ex(const void *W, const void *X, float *Y, int64_t M, int64_t N,
+                               int64_t K, rocmfp4_variant variant, rocmfp4_act act,
+                               rocmfp4_stream_t stream);
+
+/* Dense weights: out[n*K + k] = Codebook10[q] * hs(e) for every weight,
+ * written as fp32, bf16 or fp16.  Every value is exactly representable in
+ * all three types, so the result is exact; code 8 gives +0. */
+rocmfp4_status rocmfp4_dequant(const void *W, void *out, rocmfp4_out_dtype out_dtype, int64_t N,
+                               int64_t K, rocmfp4_variant variant, rocmfp4_stream_t stream);
+
+/* Row validation ("Scale Format": non-finite scale bytes are rejected).
+ * Scans every scale byte; returns ROCMFP4_OK when all are finite, else
+ * ROCMFP4_ERR_INVALID_SCALE.  *first_bad_block (may be NULL) receives the
+ * row-major block index n*(K/32)+b of the first offending block, or -1.
+ * Synchronises with the stream before returning. */
+rocmfp4_status rocmfp4_validate(const void *W, int64_t N, int64_t K, rocmfp4_variant variant,
+                                int64_t *first_bad_block, rocmfp4_stream_t stream);
+
+/* Error bits recorded by kernels on the current device since the last query
+ * (bit 0: a kernel gave up waiting for its own bulk copies, so its outputs
+ * are invalid).  Synchronises with the stream, clears the bits, and on a
+ * non-zero result also clears the split-reduction counters.  Returns
+ * 0xFFFFFFFF if the query itself failed. */
+uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream);
+
+/* Static name of a status code. */
+const char *rocmfp4_status_string(rocmfp4_status status);
+
+/* Message of the last failure seen by this thread ("" if none). */
+const char *rocmfp4_last_error(void);
+
+/* Number of device kernels this library has launched in this process
+ * (a counter kept by the host wrappers; used by the benchmark). */
+uint64_t rocmfp4_launch_count(void);
+
+/* Free the per-device workspaces.  Calls made afterwards recreate them. */
+void rocmfp4_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROCMFP4_H_ */
