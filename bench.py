@@ -153,28 +153,37 @@ def max_over_ranks(value: float, world: int) -> float:
 # ---- CPU oracle baseline ------------------------------------------------------------------
 
 def cpu_oracle_rate(mats, variant, M, budget_s=12.0, act=0):
-    """Times the oracle on row samples of each matrix; returns (GB/s of the metric, cores, sample text)."""
+    """Times the oracle on row samples of each matrix; returns (GB/s of the metric, cores, sample text, seconds).
+
+    The sample size is chosen from a short probe so that the timed run takes
+    about budget_s seconds; the metric counts the sampled rows' packed bytes
+    plus their share of activation and output bytes."""
     import oracle
     import synth
     cores = os.cpu_count() or 1
-    rows_per = 8
-    total_bytes, total_t, desc = 0, 0.0, []
-    # grow the sample until about budget_s seconds of CPU work
-    while True:
-        total_bytes, total_t = 0, 0.0
-        for idx, (name, N, K) in enumerate(mats):
+    inputs = []
+    for idx, (name, N, K) in enumerate(mats):
+        inputs.append((N, K, synth.activations(M, K, act, seed=0, stream=synth.act_stream(0, idx))))
+
+    def run(rows_per):
+        nbytes, secs = 0.0, 0.0
+        for idx, (N, K, Xh) in enumerate(inputs):
             rows = np.arange(min(rows_per, N))
             Wr = synth.weights(N, K, variant, seed=0, stream=synth.weight_stream(0, idx), rows=rows)
-            Xh = synth.activations(M, K, act, seed=0, stream=synth.act_stream(0, idx))
             t0 = time.perf_counter()
             oracle.gemm(Wr, Xh, len(rows), K, variant, act=act, nthreads=cores)
-            total_t += time.perf_counter() - t0
-            total_bytes += len(rows) * (K // 32) * (18 if variant == 0 else 17) + 2 * M * K * len(rows) / N + 4 * M * len(rows)
-        if total_t >= budget_s or rows_per >= 4096:
-            break
-        rows_per = int(min(4096, rows_per * max(2.0, min(8.0, budget_s / max(total_t, 1e-3)))))
-    desc = f"{rows_per} rows of each of the {len(mats)} matrices (M={M}), oracle threaded over rows"
-    return total_bytes / total_t / 1e9, cores, desc, total_t
+            secs += time.perf_counter() - t0
+            rb = (K // 32) * (18 if variant == 0 else 17)
+            nbytes += len(rows) * (rb + 4 * M) + 2 * M * K * len(rows) / N
+        return nbytes, secs
+
+    probe_rows = 2 * cores
+    b, t = run(probe_rows)
+    rows_per = int(max(probe_rows, min(min(N for _, N, _ in mats), probe_rows * budget_s / max(t, 1e-3))))
+    b, t = run(rows_per)
+    desc = (f"{rows_per} rows of each of the {len(mats)} matrices (M={M}), "
+            f"oracle threaded over rows on {cores} cores")
+    return b / t / 1e9, cores, desc, t
 
 
 # ---- GPU workloads -----------------------------------------------------------------------------
@@ -250,20 +259,30 @@ def time_steps(step_fn, steps, warmup, world):
     return a.elapsed_time(b) / 1e3
 
 
-def per_matrix_kernel_times(L: LayerStep, reps=20):
-    """Average device time of each matrix's launch (CUDA events on the launching stream)."""
+def per_matrix_kernel_times(L: LayerStep, reps=None):
+    """Average device time of each matrix's kernel: a CUDA graph of `reps` launches
+    of that matrix's product (rotating over the resident copies, so every launch
+    streams from HBM) is replayed between CUDA events on the launching stream."""
     import torch
+    reps = reps or max(8, 2 * L.copies)
     out = []
     for m, (name, N, K) in enumerate(L.mats):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        for i in range(reps):
-            r = i % L.copies
-            ev[i][0].record()
-            L.rf4.gemm(L.W[r][m], L.X[r][m], N, K, L.variant, Y=L.Y[r][m])
-            ev[i][1].record()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                r = i % L.copies
+                L.rf4.gemm(L.W[r][m], L.X[r][m], N, K, L.variant, Y=L.Y[r][m])
+        g.replay()
         torch.cuda.synchronize()
-        ms = [e0.elapsed_time(e1) for e0, e1 in ev[2:]]
-        out.append(float(np.mean(ms)) / 1e3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s = torch.cuda.current_stream()
+        e0.record(s)
+        for _ in range(3):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1) / 1e3 / (3 * reps))
+        del g
     return out
 
 

@@ -16,9 +16,9 @@ using namespace rocmfp4;
 struct DeviceState {
   bool ready = false;
   int sms = 0;
-  int occ[2][2] = {{0, 0}, {0, 0}};  // stream kernel CTAs per SM [variant][act]
+  int occ[2][2][4] = {};             // stream kernel CTAs per SM [variant][act][log2 mb]
   int64_t wmax = 0;                  // workspace capacity in warps
-  float* ws = nullptr;               // 2 * wmax records of 128 floats
+  float* ws = nullptr;               // 2 * wmax records of kStreamTileRows * 8 floats
   uint32_t* cnt = nullptr;           // wmax split counters
   uint32_t* err = nullptr;           // kernel error bits
   unsigned long long* vfirst = nullptr;
@@ -58,16 +58,19 @@ rocmfp4_status device_state(DeviceState** out) {
   if (!d.ready) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = stream_init_driver()) != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
     int best = 1;
     for (int v = 0; v < 2; ++v)
-      for (int a = 0; a < 2; ++a) {
-        if ((e = stream_prepare(v, a)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        if ((e = stream_occupancy(v, a, &d.occ[v][a])) != cudaSuccess) return cuda_fail(e, "occupancy");
-        if (d.occ[v][a] < 1) return fail(ROCMFP4_ERR_UNSUPPORTED, "streaming kernel does not fit on this device");
-        best = d.occ[v][a] > best ? d.occ[v][a] : best;
-      }
+      for (int a = 0; a < 2; ++a)
+        for (int lm = 0; lm < 4; ++lm) {
+          int& o = d.occ[v][a][lm];
+          if ((e = stream_prepare(v, a, 1 << lm)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+          if ((e = stream_occupancy(v, a, 1 << lm, &o)) != cudaSuccess) return cuda_fail(e, "occupancy");
+          if (o < 1) return fail(ROCMFP4_ERR_UNSUPPORTED, "streaming kernel does not fit on this device");
+          best = o > best ? o : best;
+        }
     d.wmax = (int64_t)d.sms * best * kStreamWarpsPerCta;
-    if ((e = cudaMalloc(&d.ws, sizeof(float) * 128 * 2 * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.ws, sizeof(float) * kStreamTileRows * 8 * 2 * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.cnt, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.err, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.vfirst, sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
@@ -84,13 +87,6 @@ rocmfp4_status check_shape(int64_t N, int64_t K, int variant) {
   if (!valid_variant(variant)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown variant");
   if (N < 0 || K < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
   if (K % 32 != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "K must be a multiple of 32");
-  return ROCMFP4_OK;
-}
-
-rocmfp4_status check_matrix(const void* W, int64_t N, int64_t K, int variant) {
-  rocmfp4_status st = check_shape(N, K, variant);
-  if (st != ROCMFP4_OK) return st;
-  if (N > 0 && K > 0 && W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
   return ROCMFP4_OK;
 }
 
@@ -113,7 +109,9 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
 
   const int64_t row_bytes = K / 32 * block_bytes_of(variant);
   const int64_t ku = stream_weights_per_unit(variant);
-  const bool stream_ok = K % ku == 0 && aligned16(W) && aligned16(X);
+  // The streaming kernel indexes units and tiles in 32 bits.
+  const bool stream_ok = K % ku == 0 && aligned16(W) && aligned16(X) &&
+                         (N + kStreamTileRows - 1) / kStreamTileRows * (K / ku) < (int64_t(1) << 31);
   const uint16_t* Xh = static_cast<const uint16_t*>(X);
   if (!stream_ok) {
     GenericArgs a{static_cast<const uint8_t*>(W), Xh, Y, N, K, row_bytes, M};
@@ -123,11 +121,14 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
     return ROCMFP4_OK;
   }
   const int64_t nspans = K / ku;
-  const int64_t units = (N + 15) / 16 * nspans;
-  const int64_t cap = (int64_t)d->sms * d->occ[variant][act] * kStreamWarpsPerCta;
-  const int64_t wact = units < cap ? units : cap;
-  const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
+  const int64_t units = (N + kStreamTileRows - 1) / kStreamTileRows * nspans;
   for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    const int mc = (int)(M - m0 < 8 ? M - m0 : 8);
+    const int mb = stream_mb_for(mc);
+    const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
+    const int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
+    const int64_t wact = units < cap ? units : cap;
+    const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
     GemvArgs a{};
     a.W = static_cast<const uint8_t*>(W);
     a.X = Xh + m0 * K;
@@ -135,7 +136,7 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
     a.N = N;
     a.K = K;
     a.row_bytes = row_bytes;
-    a.M = (int)(M - m0 < 8 ? M - m0 : 8);
+    a.M = mc;
     a.nspans = nspans;
     a.units = units;
     a.wact = wact;

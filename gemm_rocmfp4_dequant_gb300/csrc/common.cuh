@@ -15,6 +15,7 @@
 // significant bits and lies in [2^-10, 2240], inside fp16's exact range.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -59,6 +60,15 @@ RF4_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
       : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared (box of the tensor map at element
+// coordinates (x, y)), completing the box's bytes on `bar`.
+RF4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 RF4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -77,6 +87,25 @@ RF4_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > (1ll << 32)) return false;
   }
   return true;
+}
+
+// ---- programmatic dependent launch -------------------------------------------
+// Wait until the grids this one depends on have completed and their writes
+// are visible (a no-op when the launch has no programmatic dependency).
+RF4_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid on the stream to begin launching.
+RF4_DEV void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- inter-warp hand-off (split tiles) ----------------------------------------
+// Release orders this thread's earlier stores (and, through __syncwarp, its
+// warp's) before the increment; acquire orders later loads after it.
+RF4_DEV uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+RF4_DEV void store_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---- decode ------------------------------------------------------------------

@@ -37,7 +37,8 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ W, void* __restrict__
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t byte = __ldg(b + j0 + i);
-      v[i] = codebook10(h ? (byte >> 4) : (byte & 15u)) * hs;
+      // + 0 turns the -0 of a negative code times a zero scale into +0
+      v[i] = __fadd_rn(codebook10(h ? (byte >> 4) : (byte & 15u)) * hs, 0.0f);
     }
     const int64_t o = blk * 32 + 16 * h + j0;
     if constexpr (OUT == 0) {

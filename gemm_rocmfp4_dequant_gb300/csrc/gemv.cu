@@ -7,15 +7,16 @@
 // explains how the Blackwell e2m1/e4m3 conversions reproduce it exactly.
 //
 // Work decomposition (stream-K over warps).  The matrix is cut into units of
-// 16 rows x SPAN bytes (8 dual blocks = 144 B, or 16 single-scale blocks =
+// 32 rows x SPAN bytes (8 dual blocks = 144 B, or 16 single-scale blocks =
 // 272 B, per row).  Units are ordered tile-major (all K spans of rows 0..15,
 // then rows 16..31, ...) and every active warp of a persistent grid takes an
 // equal contiguous range of them, so every warp streams the same number of
 // bytes.  A warp streams its units through a private ring of shared-memory
-// stages filled by 1-D bulk copies (one per row, lanes 0..15), one mbarrier
-// per stage.
+// stages filled by 1-D bulk copies (one per row, plus one per activation
+// row for the unit's K span), one mbarrier per stage.
 //
-// Per unit, lane (q = lane/4, c = lane%4) owns rows q and q+8 and the
+// Per unit, lane (q = lane/4, c = lane%4) owns rows q, q+8, q+16, q+24 (two
+// m16 tiles that share every B fragment) and the
 // 4-byte-aligned lane span c (BPL whole blocks) of each row.  Each block is
 // eight mma.m16n8k16 steps: step s feeds qs bytes 2s and 2s+1 of the lane's
 // block; each byte becomes one f16x2 A register (low nibble -> weight 2s or
@@ -25,12 +26,14 @@
 // round-to-nearest fp32 registers after every block (8 MMAs), so the tensor
 // core's own accumulation never runs long.
 //
-// A tile (16 rows) whose units are split between warps is finished by its
-// last-arriving warp: each contributor writes its 16 x 8 partial to the
+// A tile (32 rows) whose units are split between warps is finished by its
+// last-arriving warp: each contributor writes its 32 x 8 partial to the
 // workspace, fences, and bumps a per-tile counter; the warp that completes
 // the count sums all partials in warp (= K) order, writes Y and resets the
 // counter.  Nobody waits and the sum order is fixed, so results are bitwise
 // reproducible.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,16 +41,24 @@ namespace rocmfp4 {
 namespace {
 
 constexpr int kWarps = kStreamWarpsPerCta;
+constexpr int kTileRows = 32;  // rows per unit / tile: two m16 MMA tiles sharing each B fragment
 
-template <int V>
-constexpr int stages() { return V == 0 ? 6 : 4; }
+// Per-warp ring stage: 32 weight rows x SPAN bytes, then the matching slice of
+// MB activation rows (MB >= M, rounded to 1, 2, 4 or 8), KU fp16/bf16 values each.
+template <int V, int MB>
+constexpr int stage_bytes() { return kTileRows * Fmt<V>::SPAN + MB * Fmt<V>::KU * 2; }
 
-template <int V>
-constexpr int stage_bytes() { return 16 * Fmt<V>::SPAN; }
+// Stages per warp: as many as fit in about 54 KB per CTA (four CTAs, 16 warps
+// per SM), at least 2 (one unit in flight while the previous one computes).
+template <int V, int MB>
+constexpr int stages() {
+  constexpr int n = (54 * 1024) / (kWarps * stage_bytes<V, MB>());
+  return n < 2 ? 2 : (n > 8 ? 8 : n);
+}
 
-template <int V>
+template <int V, int MB>
 constexpr size_t smem_bytes() {
-  return (size_t)kWarps * stages<V>() * stage_bytes<V>() + (size_t)kWarps * stages<V>() * 8;
+  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8;
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -85,133 +96,125 @@ RF4_DEV uint32_t weight_pair(uint32_t codes_f16x2, uint32_t s2) {
   return w;
 }
 
-template <int V, int ACT>
-__global__ void __launch_bounds__(kWarps * 32) gemv_stream_kernel(const GemvArgs p) {
+// Copies of unit (t, j) into a stage: one 2-D tensor copy of the 32 x SPAN
+// weight box (rows past N arrive as zeros) by lane 0, which also arms the
+// stage's barrier for the whole unit; then lanes 0..M-1 copy the unit's slice
+// of one activation row each (issue_x).
+template <int V, int MB>
+__device__ __forceinline__ void issue_w(const CUtensorMap* tmw, int M, int t, int j, uint8_t* stage, uint32_t bar,
+                                        int lane) {
   using F = Fmt<V>;
-  constexpr int NS = stages<V>();
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(kTileRows * F::SPAN + M * F::KU * 2));
+    tma_load_2d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * kTileRows, bar);
+  }
+}
+
+template <int V, int MB>
+__device__ __forceinline__ void issue_x(const uint16_t* __restrict__ X, int64_t K, int M, int j, uint8_t* stage,
+                                        uint32_t bar, int lane) {
+  using F = Fmt<V>;
+  constexpr int XROW = F::KU * 2;
+  if (lane < M)
+    bulk_g2s(smem_addr(stage + kTileRows * F::SPAN + lane * XROW), X + (int64_t)lane * K + (int64_t)j * F::KU, XROW,
+             bar);
+}
+
+template <int V, int ACT, int MB>
+__global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvArgs p,
+                                                                  const __grid_constant__ CUtensorMap tmw) {
+  using F = Fmt<V>;
+  constexpr int NS = stages<V, MB>();
+  constexpr int SB = stage_bytes<V, MB>();
   constexpr int SW = F::SW;
+  constexpr int XROW = F::KU * 2;  // bytes of one staged activation row
   extern __shared__ __align__(128) uint8_t smem[];
+
+  // Scalars copied out of the parameter block (nothing below takes its address).
+  const uint16_t* __restrict__ X = p.X;
+  float* __restrict__ Y = p.Y;
+  float* __restrict__ ws = p.ws;
+  uint32_t* __restrict__ cnt = p.cnt;
+  const int64_t N = p.N, K = p.K, U = p.units, S = p.nspans, wact = p.wact;
+  const int M = p.M;
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;
-  if (wg >= p.wact) return;
+  if (wg >= wact) return;
 
-  uint8_t* ring = smem + (size_t)warp * NS * stage_bytes<V>();
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * stage_bytes<V>()) + warp * NS;
+  uint8_t* ring = smem + (size_t)warp * NS * SB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * SB) + warp * NS;
 
-  const int64_t U = p.units, S = p.nspans;
-  const int64_t u0 = U * wg / p.wact, u1 = U * (wg + 1) / p.wact;
-  const int64_t nunits = u1 - u0;
-  const int64_t t_first = u0 / S;
+  // This warp's units [u0, u1); (t, j) = (tile, span) of a unit is tracked
+  // incrementally so that the loops do no integer division.
+  const int64_t u0 = U * wg / wact, u1 = U * (wg + 1) / wact;
+  const int nunits = (int)(u1 - u0);
+  const int t_first = (int)(u0 / S), j_first = (int)(u0 % S);
+  const int Si = (int)S;
 
   if (lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
     for (int i = 0; i < NS; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
   __syncwarp();
-
-  auto issue = [&](int64_t u, int st) {
-    const int64_t t = u / S, j = u % S;
-    const int64_t row0 = t * 16;
-    const int nvalid = (int)(p.N - row0 < 16 ? p.N - row0 : 16);
-    const uint32_t bar = smem_addr(&bars[st]);
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * F::SPAN));
-    __syncwarp();
-    if (lane < nvalid) {
-      const uint8_t* src = p.W + (row0 + lane) * p.row_bytes + j * F::SPAN;
-      bulk_g2s(smem_addr(ring + (size_t)st * stage_bytes<V>() + lane * F::SPAN), src, F::SPAN, bar);
+  // Weights do not depend on earlier kernels: start streaming them, then wait
+  // for the preceding grid (programmatic dependent launch) before touching
+  // activations, outputs or the split-reduction workspace.
+  int ti = t_first, ji = j_first;  // (tile, span) of the next unit to issue
+  for (int i = 0; i < NS - 1 && i < nunits; ++i) {
+    issue_w<V, MB>(&tmw, M, ti, ji, ring + (size_t)i * SB, smem_addr(&bars[i]), lane);
+    if (++ji == Si) { ji = 0; ++ti; }
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  __syncwarp();
+  {
+    int jx = j_first;
+    for (int i = 0; i < NS - 1 && i < nunits; ++i) {
+      issue_x<V, MB>(X, K, M, jx, ring + (size_t)i * SB, smem_addr(&bars[i]), lane);
+      if (++jx == Si) jx = 0;
     }
-  };
+  }
 
   const int q = lane >> 2, c = lane & 3;
-  const bool bcol = q < p.M;  // this lane holds B column q
-  const uint16_t* xrow = p.X + (int64_t)(bcol ? q : 0) * p.K;
+  const bool bcol = q < M;  // this lane holds B column q (activation row q)
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // acc[mt][r]: m-tile mt, D element r (rows q / q+8, columns 2c / 2c+1)
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 
-  // Writes this warp's sums for tile t (spans [js, je)), finishing the tile
-  // if this warp is its last contributor.
-  auto finish_tile = [&](int64_t t, int64_t js, int64_t je) {
-    const int64_t ra = t * 16 + q, rb = ra + 8;
-    const int c0 = 2 * c, c1 = 2 * c + 1;
-    float v[4] = {acc[0], acc[1], acc[2], acc[3]};
-    bool store = true;
-    if (!(js == 0 && je == S)) {
-      const int slot = (t == t_first) ? 0 : 1;
-      float* rec = p.ws + (2 * wg + slot) * 128;
-      rec[q * 8 + c0] = v[0];
-      rec[q * 8 + c1] = v[1];
-      rec[(q + 8) * 8 + c0] = v[2];
-      rec[(q + 8) * 8 + c1] = v[3];
-      __threadfence();
-      __syncwarp();
-      const int64_t wf = owner_of(t * S, U, p.wact), wl = owner_of(t * S + S - 1, U, p.wact);
-      uint32_t old = 0;
-      if (lane == 0) old = atomicAdd(&p.cnt[wf], 1u);
-      old = __shfl_sync(0xffffffffu, old, 0);
-      store = (int64_t)old == wl - wf;
-      if (store) {
-        __threadfence();
-        v[0] = v[1] = v[2] = v[3] = 0.f;
-        for (int64_t w2 = wf; w2 <= wl; ++w2) {
-          const int64_t tf2 = (U * w2 / p.wact) / S;
-          const float* r2 = p.ws + (2 * w2 + (t == tf2 ? 0 : 1)) * 128;
-          v[0] += __ldcg(r2 + q * 8 + c0);
-          v[1] += __ldcg(r2 + q * 8 + c1);
-          v[2] += __ldcg(r2 + (q + 8) * 8 + c0);
-          v[3] += __ldcg(r2 + (q + 8) * 8 + c1);
-        }
-        if (lane == 0) atomicExch(&p.cnt[wf], 0u);
-      }
-    }
-    if (store) {
-      if (c0 < p.M) {
-        if (ra < p.N) p.Y[c0 * p.N + ra] = v[0];
-        if (rb < p.N) p.Y[c0 * p.N + rb] = v[2];
-      }
-      if (c1 < p.M) {
-        if (ra < p.N) p.Y[c1 * p.N + ra] = v[1];
-        if (rb < p.N) p.Y[c1 * p.N + rb] = v[3];
-      }
-    }
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-  };
-
-  for (int i = 0; i < NS - 1 && i < nunits; ++i) issue(u0 + i, i);
-
-  int64_t js = u0 % S;  // first span of the current tile segment
+  int t = t_first, j = j_first;  // (tile, span) of the unit being computed
+  int js = j_first;              // first span of the current tile segment
+  int i = 0;
   bool failed = false;
-  int64_t i = 0;
   for (; i < nunits; ++i) {
-    const int64_t u = u0 + i;
-    const int st = (int)(i % NS);
-    if (i + NS - 1 < nunits) issue(u + NS - 1, (int)((i + NS - 1) % NS));
+    const int st = i % NS;
+    if (i + NS - 1 < nunits) {
+      const int sn = (i + NS - 1) % NS;
+      issue_w<V, MB>(&tmw, M, ti, ji, ring + (size_t)sn * SB, smem_addr(&bars[sn]), lane);
+      __syncwarp();
+      issue_x<V, MB>(X, K, M, ji, ring + (size_t)sn * SB, smem_addr(&bars[sn]), lane);
+      if (++ji == Si) { ji = 0; ++ti; }
+    }
     if (!mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / NS) & 1))) {
       failed = true;
       break;
     }
-    const int64_t t = u / S, j = u % S;
+    const uint8_t* stage = ring + (size_t)st * SB;
+    const uint4* xs = reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + (bcol ? q : 0) * XROW);
 
-    const uint8_t* sbase = ring + (size_t)st * stage_bytes<V>() + c * F::LANE_BYTES;
-    uint32_t wa[SW], wb[SW];
-#pragma unroll
-    for (int k = 0; k < SW; ++k) {
-      wa[k] = reinterpret_cast<const uint32_t*>(sbase + q * F::SPAN)[k];
-      wb[k] = reinterpret_cast<const uint32_t*>(sbase + (q + 8) * F::SPAN)[k];
-    }
-
+    // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or 32
+    // MMAs) and is then flushed into round-to-nearest fp32 registers.
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int phi = 0; phi < F::BPL; ++phi) {
-      const uint32_t s2a = scale_pair_at<V>(wa, phi);
-      const uint32_t s2b = scale_pair_at<V>(wb, phi);
-      const int64_t blk = j * (4 * F::BPL) + c * F::BPL + phi;
+      // 32 activations of the lane's block (block c*BPL + phi of the unit)
       uint32_t xv[16];
       if (bcol) {
-        const uint4* xs = reinterpret_cast<const uint4*>(xrow + blk * 32);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint4 v = __ldg(xs + k);
+          const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
           xv[4 * k] = v.x;
           xv[4 * k + 1] = v.y;
           xv[4 * k + 2] = v.z;
@@ -221,79 +224,226 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_stream_kernel(const GemvArgs
 #pragma unroll
         for (int k = 0; k < 16; ++k) xv[k] = 0u;
       }
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
+      uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
+      const uint8_t* sb = stage + c * F::LANE_BYTES;
+#pragma unroll
+      for (int k = 0; k < SW; ++k) {
+        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      }
+      const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
+      const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int pos = phi * F::BB + 2 * s;
-        uint32_t a[4];
-        a[0] = weight_pair<ACT>(e2m1x2_at(wa, pos), s2a);
-        a[1] = weight_pair<ACT>(e2m1x2_at(wb, pos), s2b);
-        a[2] = weight_pair<ACT>(e2m1x2_at(wa, pos + 1), s2a);
-        a[3] = weight_pair<ACT>(e2m1x2_at(wb, pos + 1), s2b);
         // B rows (2c, 2c+1) = (x[2s], x[2s+16]); rows (2c+8, 2c+9) = (x[2s+1], x[2s+17]).
         const uint32_t b0 = __byte_perm(xv[s], xv[8 + s], 0x5410);
         const uint32_t b1 = __byte_perm(xv[s], xv[8 + s], 0x7632);
-        mma16816(d, a, b0, b1, ACT == 1);
+        uint32_t a[4];
+        a[0] = weight_pair<ACT>(e2m1x2_at(w0, pos), s0);
+        a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
+        a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
+        a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
+        mma16816(d0, a, b0, b1, ACT == 1);
+        a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
+        a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
+        a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
+        a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
+        mma16816(d1, a, b0, b1, ACT == 1);
       }
-      acc[0] += d[0];
-      acc[1] += d[1];
-      acc[2] += d[2];
-      acc[3] += d[3];
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      acc[0][r] += d0[r];
+      acc[1][r] += d1[r];
     }
     __syncwarp();
     fence_proxy_async();
 
-    const bool tile_end = (j == S - 1) || (i == nunits - 1);
-    if (tile_end) {
-      finish_tile(t, js, j + 1);
+    if (j == Si - 1 || i == nunits - 1) {
+      // Tile t done for this warp (spans [js, j]): store, or hand over a partial.
+      const int c0 = 2 * c, c1 = 2 * c + 1;
+      bool store = true;
+      if (!(js == 0 && j == Si - 1)) {
+        float* rec = ws + (2 * wg + (t == t_first ? 0 : 1)) * (kTileRows * 8);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r0 = mt * 16 + q;
+          rec[r0 * 8 + c0] = acc[mt][0];
+          rec[r0 * 8 + c1] = acc[mt][1];
+          rec[(r0 + 8) * 8 + c0] = acc[mt][2];
+          rec[(r0 + 8) * 8 + c1] = acc[mt][3];
+        }
+        __syncwarp();  // orders the warp's partial stores before lane 0's release
+        const int64_t tS = (int64_t)t * S;
+        const int64_t wf = owner_of(tS, U, wact), wl = owner_of(tS + S - 1, U, wact);
+        uint32_t old = 0;
+        if (lane == 0) old = atomic_add_acq_rel_gpu(&cnt[wf], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
+        store = (int64_t)old == wl - wf;
+        if (store) {
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+          // Every contributor after the first starts inside tile t (its record
+          // is slot 0); the first one is in slot 1 if it started before the
+          // tile.  Records are read 4 at a time (independent loads in flight),
+          // then added in contributor (= K) order.
+          const bool first_in_slot1 = U * wf / wact < tS;
+          for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
+            float v[4][2][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int64_t w2 = w0 + k;
+              if (w2 <= wl) {
+                const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
+                const float* r2 = ws + (2 * w2 + slot) * (kTileRows * 8);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                  const int r0 = mt * 16 + q;
+                  v[k][mt][0] = __ldcg(r2 + r0 * 8 + c0);
+                  v[k][mt][1] = __ldcg(r2 + r0 * 8 + c1);
+                  v[k][mt][2] = __ldcg(r2 + (r0 + 8) * 8 + c0);
+                  v[k][mt][3] = __ldcg(r2 + (r0 + 8) * 8 + c1);
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (w0 + k <= wl)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) acc[mt][r] += v[k][mt][r];
+          }
+          __syncwarp();
+          if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
+        }
+      }
+      if (store) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
+          if (c0 < M) {
+            if (ra < N) Y[c0 * N + ra] = acc[mt][0];
+            if (rb < N) Y[c0 * N + rb] = acc[mt][2];
+          }
+          if (c1 < M) {
+            if (ra < N) Y[c1 * N + ra] = acc[mt][1];
+            if (rb < N) Y[c1 * N + rb] = acc[mt][3];
+          }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
       js = 0;
     }
+    if (++j == Si) { j = 0; ++t; }
   }
 
   if (failed) {
     if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
     // Let every copy already issued land before the shared memory is released.
-    for (int64_t k = i; k < nunits && k < i + NS; ++k)
+    for (int k = i; k < nunits && k < i + NS; ++k)
       (void)mbar_wait_bounded(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1));
   }
 }
 
+// Kernel instance for (variant, activation type, staged activation rows).
 template <int V, int ACT>
-const void* stream_kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT>);
+const void* kernel_for_mb(int mb) {
+  switch (mb) {
+    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1>);
+    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2>);
+    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4>);
+    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8>);
+  }
 }
 
-const void* stream_kernel(int variant, int act) {
-  if (variant == 0) return act == 0 ? stream_kernel_ptr<0, 0>() : stream_kernel_ptr<0, 1>();
-  return act == 0 ? stream_kernel_ptr<1, 0>() : stream_kernel_ptr<1, 1>();
+const void* stream_kernel(int variant, int act, int mb) {
+  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0>(mb) : kernel_for_mb<0, 1>(mb);
+  return act == 0 ? kernel_for_mb<1, 0>(mb) : kernel_for_mb<1, 1>(mb);
+}
+
+template <int V>
+size_t smem_for_mb(int mb) {
+  switch (mb) {
+    case 1: return smem_bytes<V, 1>();
+    case 2: return smem_bytes<V, 2>();
+    case 4: return smem_bytes<V, 4>();
+    default: return smem_bytes<V, 8>();
+  }
 }
 
 }  // namespace
 
+int stream_mb_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
 int stream_weights_per_unit(int variant) { return variant == 0 ? Fmt<0>::KU : Fmt<1>::KU; }
 
-size_t stream_smem_bytes(int variant) { return variant == 0 ? smem_bytes<0>() : smem_bytes<1>(); }
+size_t stream_smem_bytes(int variant, int mb) { return variant == 0 ? smem_for_mb<0>(mb) : smem_for_mb<1>(mb); }
 
-cudaError_t stream_prepare(int variant, int act) {
-  return cudaFuncSetAttribute(stream_kernel(variant, act), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)stream_smem_bytes(variant));
+cudaError_t stream_prepare(int variant, int act, int mb) {
+  return cudaFuncSetAttribute(stream_kernel(variant, act, mb), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)stream_smem_bytes(variant, mb));
 }
 
-cudaError_t stream_occupancy(int variant, int act, int* ctas_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, stream_kernel(variant, act), kWarps * 32,
-                                                       stream_smem_bytes(variant));
+cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, stream_kernel(variant, act, mb), kWarps * 32,
+                                                       stream_smem_bytes(variant, mb));
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}
+
+cudaError_t stream_init_driver() {
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorSymbolNotFound;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s) {
-  const size_t smem = stream_smem_bytes(variant);
-  if (variant == 0) {
-    if (act == 0) gemv_stream_kernel<0, 0><<<ctas, kWarps * 32, smem, s>>>(a);
-    else gemv_stream_kernel<0, 1><<<ctas, kWarps * 32, smem, s>>>(a);
-  } else {
-    if (act == 0) gemv_stream_kernel<1, 0><<<ctas, kWarps * 32, smem, s>>>(a);
-    else gemv_stream_kernel<1, 1><<<ctas, kWarps * 32, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (!g_encode) return cudaErrorInitializationError;
+  const int mb = stream_mb_for(a.M);
+  const size_t smem = stream_smem_bytes(variant, mb);
+  const int span = variant == 0 ? Fmt<0>::SPAN : Fmt<1>::SPAN;
+  // Weights as a 2-D array of 32-bit words: row_bytes/4 columns, N rows.
+  CUtensorMap tmw;
+  cuuint64_t dims[2] = {(cuuint64_t)(a.row_bytes / 4), (cuuint64_t)a.N};
+  cuuint64_t strides[1] = {(cuuint64_t)a.row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(span / 4), (cuuint32_t)kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.W), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // Programmatic dependent launch: the kernel may start (and stream weights)
+  // while the previous kernel on the stream drains; it calls
+  // griddepcontrol.wait before reading anything an earlier kernel writes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<GemvArgs*>(&a), &tmw};
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb), args);
 }
 
 }  // namespace rocmfp4

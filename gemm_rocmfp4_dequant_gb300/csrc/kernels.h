@@ -13,18 +13,21 @@ struct GemvArgs {
   int64_t N, K, row_bytes;
   int M;
   int64_t nspans;        // K / weights-per-unit
-  int64_t units;         // ceil(N/16) * nspans
+  int64_t units;         // ceil(N/32) * nspans
   int64_t wact;          // active warps (<= units)
-  float* ws;             // 2 * wact records of 16 x 8 floats
+  float* ws;             // 2 * wact records of 32 x 8 floats
   uint32_t* cnt;         // wact counters, zero between calls
   uint32_t* err;         // error bits
 };
 
 constexpr int kStreamWarpsPerCta = 4;
+constexpr int kStreamTileRows = 32;
+int stream_mb_for(int M);                   // staged activation rows: 1, 2, 4 or 8
 int stream_weights_per_unit(int variant);   // 256 (dual) or 512 (single-scale)
-size_t stream_smem_bytes(int variant);
-cudaError_t stream_prepare(int variant, int act);  // sets the dynamic smem attribute
-cudaError_t stream_occupancy(int variant, int act, int* ctas_per_sm);
+size_t stream_smem_bytes(int variant, int mb);
+cudaError_t stream_prepare(int variant, int act, int mb);  // sets the dynamic smem attribute
+cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm);
+cudaError_t stream_init_driver();           // resolves cuTensorMapEncodeTiled once
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s);
 
 // Any K % 32 == 0, any alignment: one warp per (row, column chunk).

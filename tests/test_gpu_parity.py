@@ -106,7 +106,7 @@ def test_k_zero_writes_zeros_and_empty_shapes():
     X = t.zeros((2, 0), dtype=t.float16, device="cuda")
     rf4.gemm(W, X, 5, 0, DUAL, Y=Y)
     assert t.all(Y == 0)
-    out = rf4.gemm(t.zeros(18 * 4, dtype=t.uint8, device="cuda"), t.zeros((0, 128), dtype=t.float16, device="cuda"),
+    out = rf4.gemm(t.zeros(2 * 18 * 4, dtype=t.uint8, device="cuda"), t.zeros((0, 128), dtype=t.float16, device="cuda"),
                    2, 128, DUAL)
     assert out.shape == (0, 2)
 
