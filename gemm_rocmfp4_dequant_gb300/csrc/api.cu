@@ -152,6 +152,11 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
 
 }  // namespace
 
+namespace rocmfp4 {
+void set_last_error(const std::string& message) { t_last_error = message; }
+void count_launch() { g_launches.fetch_add(1); }
+}  // namespace rocmfp4
+
 extern "C" {
 
 size_t rocmfp4_block_bytes(rocmfp4_variant variant) {

@@ -1,9 +1,14 @@
 // Host-side launch interface between api.cu and the kernel translation units.
 #pragma once
 #include <cstdint>
+#include <string>
 #include <cuda_runtime.h>
 
 namespace rocmfp4 {
+
+// Host-side bookkeeping shared by the C entry points (api.cu).
+void set_last_error(const std::string& message);  // text of rocmfp4_last_error()
+void count_launch();                              // one more kernel for rocmfp4_launch_count()
 
 // Streaming product Y[M][N] = X[M][K] . W[N][K]^T for M <= 8.
 struct GemvArgs {

@@ -109,6 +109,32 @@ rocmfp4_status rocmfp4_gemm_ex(const void *W, const void *X, float *Y, int64_t M
                                int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                rocmfp4_stream_t stream);
 
+/* Y = X . W^T for M <= 8 without allocating device memory.
+ *
+ * For callers that cannot call cudaMalloc where they run the product: an
+ * engine that has given all device memory to its own pool, code running
+ * during CUDA graph capture, or a host that forbids allocation after start-up.
+ * The paper has no counterpart; this is a deployment convenience.
+ *
+ * Same arguments, layouts and results as rocmfp4_gemm_ex (fp32 Y, fp16 or
+ * bf16 X), computed by the same streaming kernel, whose scratch (split-tile
+ * partial sums, hand-off counters, error word) is a fixed array of about
+ * 2 MiB inside the library (every GPU that loads the library holds it until
+ * the process exits) instead of a workspace allocated on first use.
+ *   - M > 8 returns ROCMFP4_ERR_UNSUPPORTED (the scratch keeps partial sums
+ *     for at most 8 activation rows), as do K not a multiple of 256 (dual)
+ *     or 512 (single-scale), and W or X not 16-byte aligned.  K == 0 writes
+ *     zeros.
+ *   - The first call on a device looks up the array's device address and
+ *     zeroes its counters (a cudaMemset and a device synchronisation, no
+ *     allocation); make that first call before any stream capture.
+ *   - Every call shares the one array per device: calls that overlap on the
+ *     GPU (different streams, or graphs replayed concurrently) race and give
+ *     wrong results.  Calls ordered on one stream are safe. */
+rocmfp4_status rocmfp4_gemm_noalloc(const void *W, const void *X, float *Y, int64_t M, int64_t N,
+                                    int64_t K, rocmfp4_variant variant, rocmfp4_act act,
+                                    rocmfp4_stream_t stream);
+
 /* Dense weights: out[n*K + k] = Codebook10[q] * hs(e) for every weight,
  * written as fp32, bf16 or fp16.  Every value is exactly representable in
  * all three types, so the result is exact; code 8 gives +0. */
