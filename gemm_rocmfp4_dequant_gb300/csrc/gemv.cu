@@ -89,6 +89,22 @@ RF4_DEV uint32_t scale_pair_at(const uint32_t (&w)[SW], int phi) {
   }
 }
 
+// Codebook10 / 2 of a byte's two codes (no scale), in the MMA operand type.
+template <int ACT>
+RF4_DEV uint32_t code_pair(uint32_t codes_f16x2) {
+  const uint32_t w = clamp5(codes_f16x2);
+  if constexpr (ACT == 1) return f16x2_to_bf16x2(w);
+  return w;
+}
+
+// E4M3 values of the scale pair of block phi of a lane span, as fp32.
+template <int V, int SW>
+RF4_DEV float2 scale_pair_f32(const uint32_t (&w)[SW], int phi) {
+  const uint32_t h = scale_pair_at<V>(w, phi);
+  const __half2 v = *reinterpret_cast<const __half2*>(&h);
+  return make_float2(__low2float(v), __high2float(v));
+}
+
 template <int ACT>
 RF4_DEV uint32_t weight_pair(uint32_t codes_f16x2, uint32_t s2) {
   const uint32_t w = hmul2(clamp5(codes_f16x2), s2);
@@ -180,6 +196,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
 
   const int q = lane >> 2, c = lane & 3;
   const bool bcol = q < M;  // this lane holds B column q (activation row q)
+  // Column-split mode (M == 1): B column q = (block of lane c', half hb) is
+  // non-zero only on lanes with q == 2c + hb.
+  constexpr bool COL = MB == 1;
+  const int hb = q & 1;
+  const bool bact = (q >> 1) == c;
+  const uint32_t sel0 = !bact ? 0x4444u : (hb ? 0x1044u : 0x4410u);  // (x[2s], 0) or (0, x[2s+16])
+  const uint32_t sel1 = !bact ? 0x4444u : (hb ? 0x3244u : 0x4432u);  // (x[2s+1], 0) or (0, x[2s+17])
 
   // acc[mt][r]: m-tile mt, D element r (rows q / q+8, columns 2c / 2c+1)
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -204,78 +227,163 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
     const uint8_t* stage = ring + (size_t)st * SB;
     const uint4* xs = reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + (bcol ? q : 0) * XROW);
 
-    // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or 32
-    // MMAs) and is then flushed into round-to-nearest fp32 registers.
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (COL) {
+      // M == 1, column split: B column n = 2c' + h holds x only for the k rows
+      // of lane c''s block and half h, so D[row][2c + h] is the half-block sum
+      // sum_i (Codebook10[q_i] / 2) * x_i of lane c's block.  Lane (q, c) thus
+      // holds exactly its own block's half sums for rows q, q+8 (per m-tile),
+      // and applies the scales once per half-block in fp32.
 #pragma unroll
-    for (int phi = 0; phi < F::BPL; ++phi) {
-      // 32 activations of the lane's block (block c*BPL + phi of the unit)
-      uint32_t xv[16];
-      if (bcol) {
+      for (int phi = 0; phi < F::BPL; ++phi) {
+        // the 16 activations of half hb of the lane's block (zeros if inactive)
+        uint32_t xh[8];
+        if (bact) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
-          xv[4 * k] = v.x;
-          xv[4 * k + 1] = v.y;
-          xv[4 * k + 2] = v.z;
-          xv[4 * k + 3] = v.w;
+          for (int k = 0; k < 2; ++k) {
+            const uint4 v = xs[(c * F::BPL + phi) * 4 + 2 * hb + k];
+            xh[4 * k] = v.x;
+            xh[4 * k + 1] = v.y;
+            xh[4 * k + 2] = v.z;
+            xh[4 * k + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) xh[k] = 0u;
         }
-      } else {
+        uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
+        const uint8_t* sb = stage + c * F::LANE_BYTES;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) xv[k] = 0u;
+        for (int k = 0; k < SW; ++k) {
+          w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+          w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+          w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+          w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+        }
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int pos = phi * F::BB + 2 * s;
+          // (x[2s] or x[2s+16], 0) / (0, ...) as selected for this lane; zeros if inactive
+          const uint32_t b0 = __byte_perm(xh[s], 0u, sel0);
+          const uint32_t b1 = __byte_perm(xh[s], 0u, sel1);
+          uint32_t a[4];
+          a[0] = code_pair<ACT>(e2m1x2_at(w0, pos));
+          a[1] = code_pair<ACT>(e2m1x2_at(w1, pos));
+          a[2] = code_pair<ACT>(e2m1x2_at(w0, pos + 1));
+          a[3] = code_pair<ACT>(e2m1x2_at(w1, pos + 1));
+          mma16816(d0, a, b0, b1, ACT == 1);
+          a[0] = code_pair<ACT>(e2m1x2_at(w2, pos));
+          a[1] = code_pair<ACT>(e2m1x2_at(w3, pos));
+          a[2] = code_pair<ACT>(e2m1x2_at(w2, pos + 1));
+          a[3] = code_pair<ACT>(e2m1x2_at(w3, pos + 1));
+          mma16816(d1, a, b0, b1, ACT == 1);
+        }
+        // E4M3 values of the scales of the lane's block, rows q, q+8, q+16, q+24
+        const float2 e0 = scale_pair_f32<V>(w0, phi), e1 = scale_pair_f32<V>(w1, phi);
+        const float2 e2 = scale_pair_f32<V>(w2, phi), e3 = scale_pair_f32<V>(w3, phi);
+        acc[0][0] = fmaf(d0[0], e0.x, acc[0][0]);
+        acc[0][1] = fmaf(d0[1], e0.y, acc[0][1]);
+        acc[0][2] = fmaf(d0[2], e1.x, acc[0][2]);
+        acc[0][3] = fmaf(d0[3], e1.y, acc[0][3]);
+        acc[1][0] = fmaf(d1[0], e2.x, acc[1][0]);
+        acc[1][1] = fmaf(d1[1], e2.y, acc[1][1]);
+        acc[1][2] = fmaf(d1[2], e3.x, acc[1][2]);
+        acc[1][3] = fmaf(d1[3], e3.y, acc[1][3]);
       }
-      // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
-      uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
-      const uint8_t* sb = stage + c * F::LANE_BYTES;
+    } else {
+      // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or
+      // 32 MMAs) and is then flushed into round-to-nearest fp32 registers.
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < SW; ++k) {
-        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
-        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
-        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
-        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      for (int phi = 0; phi < F::BPL; ++phi) {
+        // 32 activations of the lane's block (block c*BPL + phi of the unit)
+        uint32_t xv[16];
+        if (bcol) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
+            xv[4 * k] = v.x;
+            xv[4 * k + 1] = v.y;
+            xv[4 * k + 2] = v.z;
+            xv[4 * k + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) xv[k] = 0u;
+        }
+        // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
+        uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
+        const uint8_t* sb = stage + c * F::LANE_BYTES;
+#pragma unroll
+        for (int k = 0; k < SW; ++k) {
+          w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+          w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+          w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+          w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+        }
+        const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
+        const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int pos = phi * F::BB + 2 * s;
+          // B rows (2c, 2c+1) = (x[2s], x[2s+16]); rows (2c+8, 2c+9) = (x[2s+1], x[2s+17]).
+          const uint32_t b0 = __byte_perm(xv[s], xv[8 + s], 0x5410);
+          const uint32_t b1 = __byte_perm(xv[s], xv[8 + s], 0x7632);
+          uint32_t a[4];
+          a[0] = weight_pair<ACT>(e2m1x2_at(w0, pos), s0);
+          a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
+          a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
+          a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
+          mma16816(d0, a, b0, b1, ACT == 1);
+          a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
+          a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
+          a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
+          a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
+          mma16816(d1, a, b0, b1, ACT == 1);
+        }
       }
-      const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
-      const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int pos = phi * F::BB + 2 * s;
-        // B rows (2c, 2c+1) = (x[2s], x[2s+16]); rows (2c+8, 2c+9) = (x[2s+1], x[2s+17]).
-        const uint32_t b0 = __byte_perm(xv[s], xv[8 + s], 0x5410);
-        const uint32_t b1 = __byte_perm(xv[s], xv[8 + s], 0x7632);
-        uint32_t a[4];
-        a[0] = weight_pair<ACT>(e2m1x2_at(w0, pos), s0);
-        a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
-        a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
-        a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
-        mma16816(d0, a, b0, b1, ACT == 1);
-        a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
-        a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
-        a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
-        a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
-        mma16816(d1, a, b0, b1, ACT == 1);
+      for (int r = 0; r < 4; ++r) {
+        acc[0][r] += d0[r];
+        acc[1][r] += d1[r];
       }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      acc[0][r] += d0[r];
-      acc[1][r] += d1[r];
     }
     __syncwarp();
     fence_proxy_async();
 
     if (j == Si - 1 || i == nunits - 1) {
-      // Tile t done for this warp (spans [js, j]): store, or hand over a partial.
-      const int c0 = 2 * c, c1 = 2 * c + 1;
+      // Tile t done for this warp (spans [js, j]).  Bring the partial sums to
+      // lanes: in column-split mode add the two halves and the four lanes of
+      // each quad (fixed order), so lane (q, 0) holds rows q, q+8, q+16, q+24.
+      if constexpr (COL) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          float ra = acc[mt][0] + acc[mt][1], rb = acc[mt][2] + acc[mt][3];
+          ra += __shfl_xor_sync(0xffffffffu, ra, 1);
+          rb += __shfl_xor_sync(0xffffffffu, rb, 1);
+          ra += __shfl_xor_sync(0xffffffffu, ra, 2);
+          rb += __shfl_xor_sync(0xffffffffu, rb, 2);
+          acc[mt][0] = ra;  // (Codebook10 / 2) x E4M3 = Codebook10 x half-scale
+          acc[mt][2] = rb;
+          acc[mt][1] = acc[mt][3] = 0.f;
+        }
+      }
+      const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
+      const bool owner = !COL || c == 0;  // lanes holding finished values
       bool store = true;
       if (!(js == 0 && j == Si - 1)) {
         float* rec = ws + (2 * wg + (t == t_first ? 0 : 1)) * (kTileRows * 8);
+        if (owner) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int r0 = mt * 16 + q;
-          rec[r0 * 8 + c0] = acc[mt][0];
-          rec[r0 * 8 + c1] = acc[mt][1];
-          rec[(r0 + 8) * 8 + c0] = acc[mt][2];
-          rec[(r0 + 8) * 8 + c1] = acc[mt][3];
+          for (int mt = 0; mt < 2; ++mt) {
+            const int r0 = mt * 16 + q;
+            rec[r0 * 8 + c0] = acc[mt][0];
+            rec[(r0 + 8) * 8 + c0] = acc[mt][2];
+            if (!COL) {
+              rec[r0 * 8 + c1] = acc[mt][1];
+              rec[(r0 + 8) * 8 + c1] = acc[mt][3];
+            }
+          }
         }
         __syncwarp();  // orders the warp's partial stores before lane 0's release
         const int64_t tS = (int64_t)t * S;
@@ -285,46 +393,34 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
         old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
         store = (int64_t)old == wl - wf;
         if (store) {
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
-          // Every contributor after the first starts inside tile t (its record
-          // is slot 0); the first one is in slot 1 if it started before the
-          // tile.  Records are read 4 at a time (independent loads in flight),
-          // then added in contributor (= K) order.
+          // Last contributor: lane r sums row r of the tile over all records
+          // in contributor (= K) order and stores it.  Every contributor after
+          // the first starts inside tile t (record slot 0); the first is in
+          // slot 1 if it started before the tile.
           const bool first_in_slot1 = U * wf / wact < tS;
-          for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
-            float v[4][2][4];
+          const int64_t row = (int64_t)t * kTileRows + lane;
+          for (int m = 0; m < M; ++m) {
+            float sum = 0.f;
+            for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
+              float v[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int64_t w2 = w0 + k;
-              if (w2 <= wl) {
+              for (int k = 0; k < 8; ++k) {
+                const int64_t w2 = w0 + k;
                 const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-                const float* r2 = ws + (2 * w2 + slot) * (kTileRows * 8);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                  const int r0 = mt * 16 + q;
-                  v[k][mt][0] = __ldcg(r2 + r0 * 8 + c0);
-                  v[k][mt][1] = __ldcg(r2 + r0 * 8 + c1);
-                  v[k][mt][2] = __ldcg(r2 + (r0 + 8) * 8 + c0);
-                  v[k][mt][3] = __ldcg(r2 + (r0 + 8) * 8 + c1);
-                }
+                v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8 + m) : 0.f;
               }
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (w0 + k <= wl) sum += v[k];
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (w0 + k <= wl)
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                  for (int r = 0; r < 4; ++r) acc[mt][r] += v[k][mt][r];
+            if (row < N) Y[m * N + row] = sum;
           }
           __syncwarp();
           if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
         }
+        store = false;  // the last contributor stored above
       }
-      if (store) {
+      if (store && owner) {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
@@ -332,7 +428,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
             if (ra < N) Y[c0 * N + ra] = acc[mt][0];
             if (rb < N) Y[c0 * N + rb] = acc[mt][2];
           }
-          if (c1 < M) {
+          if (!COL && c1 < M) {
             if (ra < N) Y[c1 * N + ra] = acc[mt][1];
             if (rb < N) Y[c1 * N + rb] = acc[mt][3];
           }
