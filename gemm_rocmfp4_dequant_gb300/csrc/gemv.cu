@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
           // slot 1 if it started before the tile.
           const bool first_in_slot1 = U * wf / wact < tS;
           const int64_t row = (int64_t)t * kTileRows + lane;
-          for (int m = 0; m < M; ++m) {
+          if (M == 1) {
             float sum = 0.f;
             for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
               float v[8];
@@ -407,13 +407,41 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvA
               for (int k = 0; k < 8; ++k) {
                 const int64_t w2 = w0 + k;
                 const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-                v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8 + m) : 0.f;
+                v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8) : 0.f;
               }
 #pragma unroll
               for (int k = 0; k < 8; ++k)
                 if (w0 + k <= wl) sum += v[k];
             }
-            if (row < N) Y[m * N + row] = sum;
+            if (row < N) Y[row] = sum;
+          } else {
+            // the 8 column slots of row `lane` are 32 contiguous bytes per record
+            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
+              float4 v[4][2];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int64_t w2 = w0 + k;
+                const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
+                const float4* r2 = reinterpret_cast<const float4*>(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8);
+                if (w2 <= wl) {
+                  v[k][0] = __ldcg(r2);
+                  v[k][1] = __ldcg(r2 + 1);
+                } else {
+                  v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (w0 + k <= wl) {
+                  sum[0] += v[k][0].x; sum[1] += v[k][0].y; sum[2] += v[k][0].z; sum[3] += v[k][0].w;
+                  sum[4] += v[k][1].x; sum[5] += v[k][1].y; sum[6] += v[k][1].z; sum[7] += v[k][1].w;
+                }
+            }
+            if (row < N)
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                if (m < M) Y[m * N + row] = sum[m];
           }
           __syncwarp();
           if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
