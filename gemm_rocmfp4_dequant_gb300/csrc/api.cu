@@ -59,6 +59,7 @@ rocmfp4_status device_state(DeviceState** out) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if ((e = stream_init_driver()) != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+    if ((e = tc_prepare()) != cudaSuccess) return cuda_fail(e, "tensor-core kernel set-up");
     int best = 1;
     for (int v = 0; v < 2; ++v)
       for (int a = 0; a < 2; ++a)
@@ -113,7 +114,18 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
   const bool stream_ok = K % ku == 0 && aligned16(W) && aligned16(X) &&
                          (N + kStreamTileRows - 1) / kStreamTileRows * (K / ku) < (int64_t(1) << 31);
   const uint16_t* Xh = static_cast<const uint16_t*>(X);
-  if (!stream_ok) {
+  // More than 8 activation rows: the tensor-core kernel reads W once per
+  // 256-token tile instead of once per 8 rows.
+  const bool tc_ok = M > 8 && K % tc_k_multiple(variant) == 0 && aligned16(W) && aligned16(X) &&
+                     M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31);
+  if (tc_ok) {
+    TcArgs a{static_cast<const uint8_t*>(W), Xh, Y, M, N, K, row_bytes, d->err};
+    cudaError_t e = launch_gemm_tc(variant, act, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+    g_launches.fetch_add(1);
+    return ROCMFP4_OK;
+  }
+  if (!stream_ok || M > 8) {
     GenericArgs a{static_cast<const uint8_t*>(W), Xh, Y, N, K, row_bytes, M};
     cudaError_t e = launch_gemm_generic(variant, act, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "generic kernel launch");

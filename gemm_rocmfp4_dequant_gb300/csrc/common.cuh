@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 
 #define RF4_DEV __device__ __forceinline__
+#define RF4_HOSTDEV __host__ __device__ __forceinline__
 
 namespace rocmfp4 {
 

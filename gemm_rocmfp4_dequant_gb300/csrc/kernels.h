@@ -35,6 +35,20 @@ cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm);
 cudaError_t stream_init_driver();           // resolves cuTensorMapEncodeTiled once
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s);
 
+// Tensor-core product Y[M][N] = X[M][K] . W[N][K]^T (tcgen05, decoded weights
+// in tensor memory).  Needs K % tc_k_multiple(variant) == 0, W and X 16-byte
+// aligned, and M, N, K below 2^31.
+struct TcArgs {
+  const uint8_t* W;
+  const uint16_t* X;
+  float* Y;
+  int64_t M, N, K, row_bytes;
+  uint32_t* err;
+};
+int tc_k_multiple(int variant);   // 256 (dual) or 512 (single-scale)
+cudaError_t tc_prepare();         // resolves cuTensorMapEncodeTiled, sets the smem attributes
+cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s);
+
 // Any K % 32 == 0, any alignment: one warp per (row, column chunk).
 struct GenericArgs {
   const uint8_t* W;
