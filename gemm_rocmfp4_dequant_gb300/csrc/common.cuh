@@ -70,6 +70,23 @@ RF4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_
       : "memory");
 }
 
+// 2-D tiled tensor copy shared -> global of the box at (x, y); elements
+// outside the tensor are not written.  Part of the thread's bulk group.
+RF4_DEV void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+RF4_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read their source.
+template <int N>
+RF4_DEV void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+RF4_DEV void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 RF4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -35,14 +35,17 @@
 //   warp 1       tensor-memory allocation and the MMA issue (one thread)
 //   warp 2       TMA producer of raw ROCmFP4 chunks (128 rows x 256 or 512 K)
 //   warp 3       idle after set-up
-//   warps 4-11   decode: warp w handles rows 32*(w % 4) .. +31 and block
-//                (w - 4) / 4 of each 64-K slice (one thread per row)
+//   warps 4-11   decode: warp w handles rows 32*(w % 4) .. +31 (one thread
+//                per row) of the 64-K slices of parity (w - 4) / 4, so two
+//                slices are decoded at once
 //   warps 12-15  chain folds and the epilogue (tensor-memory lanes 32*(w % 4))
 // A stage (X slice + decoded A slice) is released by one tcgen05.commit.
 // Every wait is bounded: a warp that gives up records kErrWaitTimeout and
 // leaves its loops, and all warps still meet at the final barrier that
 // precedes the tensor-memory release.
 #include <cudaTypedefs.h>
+
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -70,7 +73,9 @@ struct TcFmt {
   static constexpr int SUBS = KR / kSubK;                 // 64-K slices per chunk: 4 / 8
   static constexpr int RSTAGES = V == 0 ? 3 : 2;         // raw chunk ring
   static constexpr int RBYTES = kTcRows * RSPAN;         // one raw stage
+  static constexpr int EBUF = V == 0 ? 2 : 1;            // epilogue buffers per output warp
 };
+constexpr uint32_t kEpiBytes = 16 * 32 * 4;  // one epilogue buffer: 16 tokens x 32 outputs, fp32
 
 // Shared- and tensor-memory plan for a token-tile width nt (multiple of 16, <= 256).
 struct TcPlan {
@@ -78,6 +83,7 @@ struct TcPlan {
   uint32_t sbytes;      // one stage: X slice + decoded A slice
   uint32_t stages;      // stage ring depth
   uint32_t off_raw;     // raw ring
+  uint32_t off_epi;     // epilogue buffers
   uint32_t off_bar;     // mbarriers
   uint32_t smem;        // dynamic bytes requested (with 1 KB alignment slack)
   uint32_t cstride;     // tensor-memory columns per accumulator slot
@@ -89,11 +95,13 @@ RF4_HOSTDEV TcPlan tc_plan(int variant, int nt) {
   p.xbytes = (uint32_t)nt * 128u;
   p.sbytes = p.xbytes + kABytes;
   const uint32_t raw = variant == 0 ? TcFmt<0>::RSTAGES * TcFmt<0>::RBYTES : TcFmt<1>::RSTAGES * TcFmt<1>::RBYTES;
-  const uint32_t fixed = raw + 512 + 1024;  // raw ring, barriers, alignment slack
+  const uint32_t epi = 4u * kEpiBytes * (variant == 0 ? TcFmt<0>::EBUF : TcFmt<1>::EBUF);
+  const uint32_t fixed = raw + epi + 512 + 1024;  // raw ring, epilogue buffers, barriers, alignment slack
   uint32_t s = (kSmemBudget - fixed) / p.sbytes;
   p.stages = s > (uint32_t)kMaxStages ? (uint32_t)kMaxStages : s;
   p.off_raw = p.stages * p.sbytes;
-  p.off_bar = p.off_raw + raw;
+  p.off_epi = p.off_raw + raw;
+  p.off_bar = p.off_epi + epi;
   p.smem = p.off_bar + 512 + 1024;
   p.cstride = nt <= 128 ? 128u : 256u;
   p.tmem_cols = 2 * p.cstride;
@@ -253,31 +261,37 @@ struct Bars {
   uint64_t* accfree;  // epilogue has read R and C (output warps)
 };
 
-// One block of one 64-K slice: block HALF of slice S of the raw chunk, for
-// this thread's weight row, into its 128-byte row of the A slice.
-template <int V, int ACT, int S, int HALF>
-RF4_DEV void decode_block_to_smem(const uint8_t* rrow, uint8_t* arow, int row) {
+// Slice S (two blocks, 64 K) of the raw chunk, for this thread's weight row,
+// into its 128-byte row of the A slice (16-byte chunk c stored at c ^ (row % 8)).
+template <int V, int ACT, int S>
+RF4_DEV void decode_slice_to_smem(const uint8_t* rrow, uint8_t* arow, int row) {
   using F = TcFmt<V>;
-  constexpr int lo = (2 * S + HALF) * F::BB;  // first byte of the block in the chunk row
-  constexpr int a0 = lo / 16 * 16;            // 16-byte aligned 32-byte window
-  static_assert(a0 + 32 <= F::RSPAN && lo - a0 + F::BB <= 32, "block window");
-  uint32_t w[8];
+  constexpr int lo = 2 * S * F::BB;  // first byte of the slice's two blocks in the chunk row
+  constexpr int a0 = lo / 16 * 16;   // 16-byte aligned 48-byte window
+  static_assert(a0 + 48 <= F::RSPAN && lo - a0 + 2 * F::BB <= 48, "slice window");
+  uint32_t w[12];
   const uint4* src = reinterpret_cast<const uint4*>(rrow + a0);
-  const uint4 v0 = src[0], v1 = src[1];
-  w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-  w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-  uint32_t out[16];
-  decode_block<V, ACT>(w, lo - a0, out);
-  // 32 K values = four 16-byte chunks (4*HALF .. 4*HALF+3) of the 128-byte row, swizzled
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int chunk = (4 * HALF + c) ^ (row & 7);
-    *reinterpret_cast<uint4*>(arow + chunk * 16) = make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+  for (int q = 0; q < 3; ++q) {
+    const uint4 v = src[q];
+    w[4 * q] = v.x;
+    w[4 * q + 1] = v.y;
+    w[4 * q + 2] = v.z;
+    w[4 * q + 3] = v.w;
+  }
+  uint32_t out0[16], out1[16];
+  decode_block<V, ACT>(w, lo - a0, out0);
+  decode_block<V, ACT>(w, lo - a0 + F::BB, out1);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t* o = c < 4 ? out0 + 4 * c : out1 + 4 * (c - 4);
+    *reinterpret_cast<uint4*>(arow + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-// Slices S .. SUBS-1 of one raw chunk; false if a wait gave up.
-template <int V, int ACT, int HALF, int S = 0>
+// The slices of parity HALF of one raw chunk (the other decode set takes the
+// rest); false if a wait gave up.  The ring advances over every slice.
+template <int V, int ACT, int HALF, int S = HALF>
 RF4_DEV bool decode_chunk(const uint8_t* rrow, uint8_t* abase, uint32_t sbytes, uint32_t stages, int row, int lane,
                           Ring& ring, const Bars& b, uint32_t rempty_bar) {
   if constexpr (S >= TcFmt<V>::SUBS) {
@@ -288,8 +302,8 @@ RF4_DEV bool decode_chunk(const uint8_t* rrow, uint8_t* abase, uint32_t sbytes, 
     // first one, which counts as complete).
     if (!warp_wait(smem_addr(&b.empty[ring.stage]), ring.phase ^ 1u)) return false;
     uint8_t* arow = abase + (size_t)ring.stage * sbytes + (size_t)row * 128;
-    decode_block_to_smem<V, ACT, S, HALF>(rrow, arow, row);
-    if constexpr (S + 1 == TcFmt<V>::SUBS) {
+    decode_slice_to_smem<V, ACT, S>(rrow, arow, row);
+    if constexpr (S + 2 >= TcFmt<V>::SUBS) {
       __syncwarp();
       if (lane == 0) mbar_arrive(rempty_bar);  // the warp's last read of the chunk
     }
@@ -297,15 +311,16 @@ RF4_DEV bool decode_chunk(const uint8_t* rrow, uint8_t* abase, uint32_t sbytes, 
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&b.full[ring.stage]));
     ring.next(stages);
-    return decode_chunk<V, ACT, HALF, S + 1>(rrow, abase, sbytes, stages, row, lane, ring, b, rempty_bar);
+    ring.next(stages);
+    return decode_chunk<V, ACT, HALF, S + 2>(rrow, abase, sbytes, stages, row, lane, ring, b, rempty_bar);
   }
 }
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
-                   float* __restrict__ Y, int M, int N, int K, int nt, int mtiles, int ntiles, int group_m,
-                   uint32_t* __restrict__ err) {
+                   const __grid_constant__ CUtensorMap tmy, int tma_y, float* __restrict__ Y, int M, int N, int K,
+                   int nt, int mtiles, int ntiles, int group_m, uint32_t* __restrict__ err) {
   using F = TcFmt<V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < S; ++i) {
-      mbar_init(smem_addr(&b.full[i]), 1 + kDecWarps);
+      mbar_init(smem_addr(&b.full[i]), 1 + kDecWarps / 2);  // X bytes + the 4 warps of one decode set
       mbar_init(smem_addr(&b.empty[i]), 1);
     }
     for (int i = 0; i < F::RSTAGES; ++i) {
@@ -443,10 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 12) {
     // ---- decode ----
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;      // block of each 64-K slice
+    const int half = (warp - 4) >> 2;      // decode set: slices of this parity
     const int row = quarter * 32 + lane;   // weight row of the tile
     uint8_t* abase = stage0 + plan.xbytes;
     Ring rr, ring;
+    if (half) ring.next(S);
     bool ok = true;
     for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
       for (int rc = 0; rc < nchunks; ++rc, rr.next(F::RSTAGES)) {
@@ -467,6 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t slot_r = tmem + lane_off, slot_c = tmem + lane_off + plan.cstride;
+    uint8_t* ebuf = smem + plan.off_epi + (uint32_t)quarter * F::EBUF * kEpiBytes;
+    int ebi = 0;
     uint32_t n_cfull = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
@@ -495,9 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_addr(b.cfree));
           continue;
         }
-        // last chain: Y = R (+ C)
-        const int n = n0 + quarter * 32 + lane;
-        const bool nvalid = n < N;
+        // last chain: Y = R (+ C), 16 tokens at a time
 #pragma unroll 1
         for (int c0 = 0; c0 < nt; c0 += 16) {
           uint32_t a[16], v[16];
@@ -512,16 +528,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_addr(b.accfree));  // both slots read: the next tile may start
           }
-          if (nvalid) {
-            float* y = Y + (size_t)(m0 + c0) * N + n;
-            const int mlim = M - (m0 + c0);
+          if (tma_y) {
+            // through shared memory: a [16 tokens][32 outputs] box, stored by TMA
+            // (rows past M and columns past N are not written)
+            uint8_t* buf = ebuf + (uint32_t)ebi * kEpiBytes;
+            if (lane == 0) bulk_wait_group_read<F::EBUF - 1>();  // the buffer's previous store has read it
+            __syncwarp();
+            float* fb = reinterpret_cast<float*>(buf);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j < mlim) y[(size_t)j * N] = __uint_as_float(a[j]);
+            for (int j = 0; j < 16; ++j) fb[j * 32 + lane] = __uint_as_float(a[j]);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              if (n0 + quarter * 32 < N && m0 + c0 < M) tma_store_2d(&tmy, n0 + quarter * 32, m0 + c0, smem_addr(buf));
+              bulk_commit_group();
+            }
+            ebi = ebi + 1 == F::EBUF ? 0 : ebi + 1;
+          } else {
+            const int n = n0 + quarter * 32 + lane;
+            if (n < N) {
+              float* y = Y + (size_t)(m0 + c0) * N + n;
+              const int mlim = M - (m0 + c0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < mlim) y[(size_t)j * N] = __uint_as_float(a[j]);
+            }
           }
         }
       }
     }
+    if (lane == 0) bulk_wait_group_all();  // the stores have left shared memory and completed
     if (!ok && lane == 0) atomicOr(err, kErrWaitTimeout);
   }
 
@@ -602,13 +638,28 @@ cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  // Y through TMA when its rows are 16-byte aligned, else plain stores.
+  CUtensorMap tmy;
+  memset(&tmy, 0, sizeof(tmy));
+  int tma_y = 0;
+  if (a.N % 4 == 0 && (reinterpret_cast<uintptr_t>(a.Y) & 15u) == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
+    cuuint32_t box[2] = {32u, 16u};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(&tmy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.Y, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    tma_y = 1;
+  }
   const TcPlan plan = tc_plan(variant, nt);
   const int64_t tiles = mtiles * ntiles;
   const int grid = (int)(tiles < g_sms ? tiles : g_sms);
   float* Y = a.Y;
   int M = (int)a.M, N = (int)a.N, K = (int)a.K, ntv = nt, mt = (int)mtiles, ntl = (int)ntiles, gm = 8;
   uint32_t* err = a.err;
-  void* args[] = {&tmx, &tmw, &Y, &M, &N, &K, &ntv, &mt, &ntl, &gm, &err};
+  void* args[] = {&tmx, &tmw, &tmy, &tma_y, &Y, &M, &N, &K, &ntv, &mt, &ntl, &gm, &err};
   return cudaLaunchKernel(tc_kernel(variant, act), dim3((unsigned)grid), dim3(kThreads), args, plan.smem, s);
 }
 
