@@ -25,10 +25,16 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
+
+
+class GemvOp(ctypes.Structure):
+    """rocmfp4_gemv_op: one product of a chain."""
+    _fields_ = [("W", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class RocmFP4Error(RuntimeError):
@@ -54,6 +60,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rocmfp4_gemm": ([vp, vp, vp, i64, i64, i64, c_int], c_int),
         "rocmfp4_gemm_ex": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemm_noalloc": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
         "rocmfp4_device_error_bits": ([vp], u32),
@@ -148,6 +155,26 @@ def gemv(W, x, N: int, K: int, variant: int = DUAL, y=None, stream=None):
     _check(load().rocmfp4_gemv_ex(_ptr(W), _ptr(x), _ptr(y), N, K, variant, _act_of(x), _stream(stream)),
            "rocmfp4_gemv_ex")
     return y
+
+
+def gemv_chain(ops, variant: int = DUAL, stream=None):
+    """Runs products in order, as gemm() for each: ops is a list of (W, X, Y, N, K)
+    with X [M, K] (all float16 or all bfloat16, one M) and Y [M, N] float32."""
+    torch = _torch()
+    if not ops:
+        return
+    M = ops[0][1].shape[0] if ops[0][1].dim() == 2 else 1
+    act = _act_of(ops[0][1])
+    arr = (GemvOp * len(ops))()
+    for i, (W, X, Y, N, K) in enumerate(ops):
+        _check_w(W, N, K, variant)
+        Xm = X.view(1, -1) if X.dim() == 1 else X
+        if not Xm.is_cuda or not Xm.is_contiguous() or tuple(Xm.shape) != (M, K) or _act_of(Xm) != act:
+            raise ValueError(f"product {i}: X must be a contiguous [M, K] CUDA tensor of the chain's dtype")
+        if Y.dtype != torch.float32 or not Y.is_contiguous() or Y.numel() < M * N:
+            raise ValueError(f"product {i}: Y must be a contiguous float32 tensor with M*N elements")
+        arr[i] = GemvOp(W.data_ptr(), Xm.data_ptr(), Y.data_ptr(), N, K)
+    _check(load().rocmfp4_gemv_chain(arr, len(ops), M, variant, act, _stream(stream)), "rocmfp4_gemv_chain")
 
 
 def dequant(W, N: int, K: int, variant: int = DUAL, out_dtype=None, out=None, stream=None):

@@ -21,6 +21,7 @@ struct DeviceState {
   float* ws = nullptr;               // 2 * wmax records of kStreamTileRows * 8 floats
   uint32_t* cnt = nullptr;           // wmax split counters
   uint32_t* err = nullptr;           // kernel error bits
+  uint32_t* gbar = nullptr;          // grid barrier counter of chained launches
   unsigned long long* vfirst = nullptr;
 };
 
@@ -74,6 +75,8 @@ rocmfp4_status device_state(DeviceState** out) {
     if ((e = cudaMalloc(&d.ws, sizeof(float) * kStreamTileRows * 8 * 2 * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.cnt, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.err, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.gbar, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(d.gbar, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaMalloc(&d.vfirst, sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(d.cnt, 0, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaMemset(d.err, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
@@ -162,6 +165,89 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
   return ROCMFP4_OK;
 }
 
+// Arguments of the streaming kernel for one product (M <= 8, stream-eligible).
+GemvArgs stream_args(const DeviceState* d, const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
+                     int variant, int64_t wact) {
+  const int64_t ku = stream_weights_per_unit(variant);
+  GemvArgs a{};
+  a.W = static_cast<const uint8_t*>(W);
+  a.X = static_cast<const uint16_t*>(X);
+  a.Y = Y;
+  a.N = N;
+  a.K = K;
+  a.row_bytes = K / 32 * block_bytes_of(variant);
+  a.M = (int)M;
+  a.nspans = K / ku;
+  a.units = (N + kStreamTileRows - 1) / kStreamTileRows * a.nspans;
+  a.wact = wact;
+  a.ws = d->ws;
+  a.cnt = d->cnt;
+  a.err = d->err;
+  return a;
+}
+
+bool chain_eligible(const rocmfp4_gemv_op& op, int64_t M, int variant) {
+  const int64_t ku = stream_weights_per_unit(variant);
+  return M >= 1 && M <= 8 && op.N > 0 && op.K > 0 && op.K % ku == 0 && aligned16(op.W) && aligned16(op.X) &&
+         (op.N + kStreamTileRows - 1) / kStreamTileRows * (op.K / ku) < (int64_t(1) << 31);
+}
+
+rocmfp4_status chain(const rocmfp4_gemv_op* ops, int count, int64_t M, int variant, int act, cudaStream_t s) {
+  if (count < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative count");
+  if (count == 0) return ROCMFP4_OK;
+  if (ops == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "ops is NULL");
+  if (!valid_act(act)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown activation type");
+  if (M < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  for (int i = 0; i < count; ++i) {
+    const rocmfp4_gemv_op& op = ops[i];
+    rocmfp4_status st = check_shape(op.N, op.K, variant);
+    if (st != ROCMFP4_OK) return fail(st, "product " + std::to_string(i) + ": " + t_last_error);
+    if (M == 0 || op.N == 0) continue;
+    if (op.Y == nullptr || (op.K > 0 && (op.W == nullptr || op.X == nullptr)))
+      return fail(ROCMFP4_ERR_INVALID_ARG, "product " + std::to_string(i) + ": NULL pointer");
+  }
+  if (M == 0) return ROCMFP4_OK;
+  DeviceState* d = nullptr;
+  rocmfp4_status st = device_state(&d);
+  if (st != ROCMFP4_OK) return st;
+  const int mb = stream_mb_for((int)(M < 8 ? M : 8));
+  const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
+  const int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
+  int i = 0;
+  while (i < count) {
+    if (ops[i].N == 0) {
+      ++i;
+      continue;
+    }
+    if (!chain_eligible(ops[i], M, variant)) {
+      st = product(ops[i].W, ops[i].X, ops[i].Y, M, ops[i].N, ops[i].K, variant, act, s);
+      if (st != ROCMFP4_OK) return st;
+      ++i;
+      continue;
+    }
+    // a run of eligible products, at most kChainOps
+    int n = 0;
+    int64_t umax = 0;
+    while (i + n < count && n < kChainOps && ops[i + n].N > 0 && chain_eligible(ops[i + n], M, variant)) {
+      const int64_t ku = stream_weights_per_unit(variant);
+      const int64_t u = (ops[i + n].N + kStreamTileRows - 1) / kStreamTileRows * (ops[i + n].K / ku);
+      umax = u > umax ? u : umax;
+      ++n;
+    }
+    const int64_t wact = umax < cap ? umax : cap;
+    const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
+    GemvArgs args[kChainOps];
+    for (int g = 0; g < n; ++g)
+      args[g] = stream_args(d, ops[i + g].W, ops[i + g].X, ops[i + g].Y, M, ops[i + g].N, ops[i + g].K, variant, wact);
+    cudaError_t e = n == 1 ? launch_gemv_stream(variant, act, args[0], ctas, s)
+                           : launch_gemv_chain(variant, act, args, n, d->gbar, ctas, s);
+    if (e != cudaSuccess) return cuda_fail(e, n == 1 ? "streaming kernel launch" : "chained streaming launch");
+    g_launches.fetch_add(1);
+    i += n;
+  }
+  return ROCMFP4_OK;
+}
+
 }  // namespace
 
 namespace rocmfp4 {
@@ -198,6 +284,11 @@ rocmfp4_status rocmfp4_gemm(const void* W, const void* X, float* Y, int64_t M, i
 rocmfp4_status rocmfp4_gemm_ex(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
                                rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
   return product(W, X, Y, M, N, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op* ops, int count, int64_t M, rocmfp4_variant variant,
+                                  rocmfp4_act act, rocmfp4_stream_t stream) {
+  return chain(ops, count, M, variant, act, reinterpret_cast<cudaStream_t>(stream));
 }
 
 rocmfp4_status rocmfp4_dequant(const void* W, void* out, rocmfp4_out_dtype out_dtype, int64_t N, int64_t K,
@@ -253,6 +344,7 @@ uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream) {
     // A kernel gave up waiting: its split counters may be left set, so clear them.
     cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
     cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
+    cudaMemsetAsync(d->gbar, 0, sizeof(uint32_t), s);
     cudaStreamSynchronize(s);
   }
   return bits;

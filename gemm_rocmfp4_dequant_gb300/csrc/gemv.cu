@@ -34,6 +34,8 @@
 // reproducible.
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,7 +60,7 @@ constexpr int stages() {
 
 template <int V, int MB>
 constexpr size_t smem_bytes() {
-  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8;
+  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8 + 16;
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -136,363 +138,551 @@ __device__ __forceinline__ void issue_x(const uint16_t* __restrict__ X, int64_t 
              bar);
 }
 
+// One product of a launch.  The tensor map views the weights as N rows of
+// row_bytes / 4 32-bit words, with a box of SPAN / 4 words x 32 rows.
+struct StreamOp {
+  CUtensorMap tmw;
+  const uint16_t* X;
+  float* Y;
+  int64_t N, K, units, nspans;
+  int64_t wact;  // warps sharing this product's units (<= units and <= the launch's warps)
+};
+
+// Parameters of a launch over NOPS products (NOPS = 1: a single product).
+template <int NOPS>
+struct StreamParams {
+  StreamOp op[NOPS];
+  float* ws;       // 2 * wact records of 32 x 8 floats
+  uint32_t* cnt;   // split-tile counters, zero between launches
+  uint32_t* err;   // error bits
+  uint32_t* gbar;  // grid barrier counter of a chain, zero between launches
+  int64_t wact;    // warps of the launch
+  int nops;
+  int M;
+};
+
+// A warp's position in its sequence of units across the products of a
+// launch: product g, the k-th of its n units of that product, and the unit's
+// (tile, span).
+struct Cursor {
+  int g, k, n, t, j;
+};
+
+// Moves the cursor to the first unit of the first product >= g in which the
+// warp owns units (g = nops when there is none).
+template <int NOPS>
+RF4_DEV void cursor_begin(Cursor& c, const StreamParams<NOPS>& p, int g, int64_t wg) {
+  for (; g < p.nops; ++g) {
+    const int64_t U = p.op[g].units, W = p.op[g].wact;
+    if (wg >= W) continue;
+    const int64_t u0 = U * wg / W, u1 = U * (wg + 1) / W;
+    if (u1 > u0) {
+      c.g = g;
+      c.k = 0;
+      c.n = (int)(u1 - u0);
+      c.t = (int)(u0 / p.op[g].nspans);
+      c.j = (int)(u0 % p.op[g].nspans);
+      return;
+    }
+  }
+  c.g = p.nops;
+  c.k = c.n = c.t = c.j = 0;
+}
+
+template <int NOPS>
+RF4_DEV void cursor_next(Cursor& c, const StreamParams<NOPS>& p, int64_t wg) {
+  if (++c.j == (int)p.op[c.g].nspans) {
+    c.j = 0;
+    ++c.t;
+  }
+  if (++c.k == c.n) cursor_begin(c, p, c.g + 1, wg);
+}
+
+// Grid-wide barrier number `gen` (1, 2, ...) of a chain.  The active warps
+// of a CTA meet on a shared-memory counter; the last of them arrives for the
+// CTA on the global counter (release: the CTA's stores of the previous
+// product, ordered before it by __syncwarp and the shared-memory
+// acquire/release chain, are published) and polls it, with back-off, until
+// all `ctas` CTAs have arrived `gen` times; the other warps poll the CTA's
+// shared-memory generation word.  Every wait gives up when a warp has
+// recorded an error or after about 2^32 cycles.
+RF4_DEV bool grid_barrier(uint32_t* gbar, uint32_t gen, uint32_t ctas, uint32_t warps_here, uint32_t* cta_count,
+                          uint32_t* cta_gen, uint32_t* err, int lane) {
+  __syncwarp();
+  int ok = 1;
+  if (lane == 0) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_addr(cta_count)) : "memory");
+    const long long t0 = clock64();
+    if (old + 1 == gen * warps_here) {
+      // last warp of the CTA: arrive on the grid counter and wait for everyone
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
+      uint32_t ns = 32;
+      while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gbar) : "memory");
+        if (v >= gen * ctas) break;
+        if ((*reinterpret_cast<volatile uint32_t*>(err) & kErrWaitTimeout) || clock64() - t0 > (1ll << 32)) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(ns);
+        ns = ns < 256 ? ns * 2 : 256;
+      }
+      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(cta_gen)), "r"(ok ? gen : 0xFFFFFFFFu)
+                   : "memory");
+    } else {
+      while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(cta_gen)) : "memory");
+        if (v == 0xFFFFFFFFu) {
+          ok = 0;
+          break;
+        }
+        if (v >= gen) break;
+        if (clock64() - t0 > (1ll << 32)) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  // Activations written by other SMs are read next through the async proxy.
+  asm volatile("fence.proxy.async;" ::: "memory");
+  __syncwarp();
+  return ok != 0;
+}
+
+// Adds one unit's products into acc (see the kernel comment for the layouts).
 template <int V, int ACT, int MB>
-__global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const GemvArgs p,
-                                                                  const __grid_constant__ CUtensorMap tmw) {
+RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2][4]) {
+  using F = Fmt<V>;
+  constexpr int SW = F::SW;
+  constexpr int XROW = F::KU * 2;
+  const int q = lane >> 2, c = lane & 3;
+  const bool bcol = q < M;  // this lane holds B column q (activation row q)
+  const uint4* xs = reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + (bcol ? q : 0) * XROW);
+  if constexpr (MB == 1) {
+    // M == 1, column split: B column n = 2c' + h holds x only for the k rows
+    // of lane c''s block and half h, so D[row][2c + h] is the half-block sum
+    // sum_i (Codebook10[q_i] / 2) * x_i of lane c's block.  Lane (q, c) thus
+    // holds exactly its own block's half sums for rows q, q+8 (per m-tile),
+    // and applies the scales once per half-block in fp32.
+    const int hb = q & 1;
+    const bool bact = (q >> 1) == c;
+    const uint32_t sel0 = !bact ? 0x4444u : (hb ? 0x1044u : 0x4410u);  // (x[2s], 0) or (0, x[2s+16])
+    const uint32_t sel1 = !bact ? 0x4444u : (hb ? 0x3244u : 0x4432u);  // (x[2s+1], 0) or (0, x[2s+17])
+#pragma unroll
+    for (int phi = 0; phi < F::BPL; ++phi) {
+      // the 16 activations of half hb of the lane's block (zeros if inactive)
+      uint32_t xh[8];
+      if (bact) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint4 v = xs[(c * F::BPL + phi) * 4 + 2 * hb + k];
+          xh[4 * k] = v.x;
+          xh[4 * k + 1] = v.y;
+          xh[4 * k + 2] = v.z;
+          xh[4 * k + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xh[k] = 0u;
+      }
+      uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
+      const uint8_t* sb = stage + c * F::LANE_BYTES;
+#pragma unroll
+      for (int k = 0; k < SW; ++k) {
+        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      }
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int pos = phi * F::BB + 2 * s;
+        // (x[2s] or x[2s+16], 0) / (0, ...) as selected for this lane; zeros if inactive
+        const uint32_t b0 = __byte_perm(xh[s], 0u, sel0);
+        const uint32_t b1 = __byte_perm(xh[s], 0u, sel1);
+        uint32_t a[4];
+        a[0] = code_pair<ACT>(e2m1x2_at(w0, pos));
+        a[1] = code_pair<ACT>(e2m1x2_at(w1, pos));
+        a[2] = code_pair<ACT>(e2m1x2_at(w0, pos + 1));
+        a[3] = code_pair<ACT>(e2m1x2_at(w1, pos + 1));
+        mma16816(d0, a, b0, b1, ACT == 1);
+        a[0] = code_pair<ACT>(e2m1x2_at(w2, pos));
+        a[1] = code_pair<ACT>(e2m1x2_at(w3, pos));
+        a[2] = code_pair<ACT>(e2m1x2_at(w2, pos + 1));
+        a[3] = code_pair<ACT>(e2m1x2_at(w3, pos + 1));
+        mma16816(d1, a, b0, b1, ACT == 1);
+      }
+      // E4M3 values of the scales of the lane's block, rows q, q+8, q+16, q+24
+      const float2 e0 = scale_pair_f32<V>(w0, phi), e1 = scale_pair_f32<V>(w1, phi);
+      const float2 e2 = scale_pair_f32<V>(w2, phi), e3 = scale_pair_f32<V>(w3, phi);
+      acc[0][0] = fmaf(d0[0], e0.x, acc[0][0]);
+      acc[0][1] = fmaf(d0[1], e0.y, acc[0][1]);
+      acc[0][2] = fmaf(d0[2], e1.x, acc[0][2]);
+      acc[0][3] = fmaf(d0[3], e1.y, acc[0][3]);
+      acc[1][0] = fmaf(d1[0], e2.x, acc[1][0]);
+      acc[1][1] = fmaf(d1[1], e2.y, acc[1][1]);
+      acc[1][2] = fmaf(d1[2], e3.x, acc[1][2]);
+      acc[1][3] = fmaf(d1[3], e3.y, acc[1][3]);
+    }
+  } else {
+    // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or
+    // 32 MMAs) and is then flushed into round-to-nearest fp32 registers.
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int phi = 0; phi < F::BPL; ++phi) {
+      // 32 activations of the lane's block (block c*BPL + phi of the unit)
+      uint32_t xv[16];
+      if (bcol) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
+          xv[4 * k] = v.x;
+          xv[4 * k + 1] = v.y;
+          xv[4 * k + 2] = v.z;
+          xv[4 * k + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) xv[k] = 0u;
+      }
+      // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
+      uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
+      const uint8_t* sb = stage + c * F::LANE_BYTES;
+#pragma unroll
+      for (int k = 0; k < SW; ++k) {
+        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      }
+      const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
+      const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int pos = phi * F::BB + 2 * s;
+        // B rows (2c, 2c+1) = (x[2s], x[2s+16]); rows (2c+8, 2c+9) = (x[2s+1], x[2s+17]).
+        const uint32_t b0 = __byte_perm(xv[s], xv[8 + s], 0x5410);
+        const uint32_t b1 = __byte_perm(xv[s], xv[8 + s], 0x7632);
+        uint32_t a[4];
+        a[0] = weight_pair<ACT>(e2m1x2_at(w0, pos), s0);
+        a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
+        a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
+        a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
+        mma16816(d0, a, b0, b1, ACT == 1);
+        a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
+        a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
+        a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
+        a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
+        mma16816(d1, a, b0, b1, ACT == 1);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      acc[0][r] += d0[r];
+      acc[1][r] += d1[r];
+    }
+  }
+}
+
+// End of tile t of product op for this warp (its spans [js, j] are in acc):
+// store the tile if the warp covered all of it, else hand its partial to the
+// split-tile reduction.  Resets acc.
+template <int MB, int NOPS>
+RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_t wg, int t, int t_first, int js,
+                         int j, int lane, float (&acc)[2][4]) {
+  constexpr bool COL = MB == 1;
+  const int M = p.M;
+  const int64_t N = op.N, S = op.nspans, U = op.units, wact = op.wact;
+  float* __restrict__ Y = op.Y;
+  float* __restrict__ ws = p.ws;
+  uint32_t* __restrict__ cnt = p.cnt;
+  const int q = lane >> 2, c = lane & 3;
+  // Bring the partial sums to lanes: in column-split mode add the two halves
+  // and the four lanes of each quad (fixed order), so lane (q, 0) holds rows
+  // q, q+8, q+16, q+24.
+  if constexpr (COL) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      float ra = acc[mt][0] + acc[mt][1], rb = acc[mt][2] + acc[mt][3];
+      ra += __shfl_xor_sync(0xffffffffu, ra, 1);
+      rb += __shfl_xor_sync(0xffffffffu, rb, 1);
+      ra += __shfl_xor_sync(0xffffffffu, ra, 2);
+      rb += __shfl_xor_sync(0xffffffffu, rb, 2);
+      acc[mt][0] = ra;  // (Codebook10 / 2) x E4M3 = Codebook10 x half-scale
+      acc[mt][2] = rb;
+      acc[mt][1] = acc[mt][3] = 0.f;
+    }
+  }
+  const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
+  const bool owner = !COL || c == 0;  // lanes holding finished values
+  bool store = true;
+  if (!(js == 0 && j == S - 1)) {
+    float* rec = ws + (2 * wg + (t == t_first ? 0 : 1)) * (kTileRows * 8);
+    if (owner) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = mt * 16 + q;
+        rec[r0 * 8 + c0] = acc[mt][0];
+        rec[(r0 + 8) * 8 + c0] = acc[mt][2];
+        if (!COL) {
+          rec[r0 * 8 + c1] = acc[mt][1];
+          rec[(r0 + 8) * 8 + c1] = acc[mt][3];
+        }
+      }
+    }
+    __syncwarp();  // orders the warp's partial stores before lane 0's release
+    const int64_t tS = (int64_t)t * S;
+    const int64_t wf = owner_of(tS, U, wact), wl = owner_of(tS + S - 1, U, wact);
+    uint32_t old = 0;
+    if (lane == 0) old = atomic_add_acq_rel_gpu(&cnt[wf], 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
+    if ((int64_t)old == wl - wf) {
+      // Last contributor: lane r sums row r of the tile over all records in
+      // contributor (= K) order and stores it.  Every contributor after the
+      // first starts inside tile t (record slot 0); the first is in slot 1 if
+      // it started before the tile.
+      const bool first_in_slot1 = U * wf / wact < tS;
+      const int64_t row = (int64_t)t * kTileRows + lane;
+      if (M == 1) {
+        float sum = 0.f;
+        for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
+          float v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int64_t w2 = w0 + k;
+            const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
+            v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8) : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (w0 + k <= wl) sum += v[k];
+        }
+        if (row < N) Y[row] = sum;
+      } else {
+        // the 8 column slots of row `lane` are 32 contiguous bytes per record
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
+          float4 v[4][2];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int64_t w2 = w0 + k;
+            const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
+            const float4* r2 = reinterpret_cast<const float4*>(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8);
+            if (w2 <= wl) {
+              v[k][0] = __ldcg(r2);
+              v[k][1] = __ldcg(r2 + 1);
+            } else {
+              v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (w0 + k <= wl) {
+              sum[0] += v[k][0].x; sum[1] += v[k][0].y; sum[2] += v[k][0].z; sum[3] += v[k][0].w;
+              sum[4] += v[k][1].x; sum[5] += v[k][1].y; sum[6] += v[k][1].z; sum[7] += v[k][1].w;
+            }
+        }
+        if (row < N)
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            if (m < M) Y[m * N + row] = sum[m];
+      }
+      __syncwarp();
+      if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
+    }
+    store = false;  // the last contributor stored above
+  }
+  if (store && owner) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
+      if (c0 < M) {
+        if (ra < N) Y[c0 * N + ra] = acc[mt][0];
+        if (rb < N) Y[c0 * N + rb] = acc[mt][2];
+      }
+      if (!COL && c1 < M) {
+        if (ra < N) Y[c1 * N + ra] = acc[mt][1];
+        if (rb < N) Y[c1 * N + rb] = acc[mt][3];
+      }
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+}
+
+// The streaming kernel over the NOPS products of a launch.  Each warp owns an
+// equal contiguous range of every product's units and streams them, product
+// after product, through its ring.  Weights never depend on earlier work, so
+// a warp keeps its ring full across product boundaries; a unit's activations
+// are copied only once everything it may depend on is complete: for the
+// first product, the preceding grid (programmatic dependent launch); for
+// product g > 0 of a chain, all warps' work on product g - 1 (grid barrier).
+// The barrier also makes the split-tile workspace free for the next product.
+template <int V, int ACT, int MB, int NOPS>
+__global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
   using F = Fmt<V>;
   constexpr int NS = stages<V, MB>();
   constexpr int SB = stage_bytes<V, MB>();
-  constexpr int SW = F::SW;
-  constexpr int XROW = F::KU * 2;  // bytes of one staged activation row
   extern __shared__ __align__(128) uint8_t smem[];
 
-  // Scalars copied out of the parameter block (nothing below takes its address).
-  const uint16_t* __restrict__ X = p.X;
-  float* __restrict__ Y = p.Y;
-  float* __restrict__ ws = p.ws;
-  uint32_t* __restrict__ cnt = p.cnt;
-  const int64_t N = p.N, K = p.K, U = p.units, S = p.nspans, wact = p.wact;
   const int M = p.M;
-
+  const int64_t wact = p.wact;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;
-  if (wg >= wact) return;
 
   uint8_t* ring = smem + (size_t)warp * NS * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * SB) + warp * NS;
-
-  // This warp's units [u0, u1); (t, j) = (tile, span) of a unit is tracked
-  // incrementally so that the loops do no integer division.
-  const int64_t u0 = U * wg / wact, u1 = U * (wg + 1) / wact;
-  const int nunits = (int)(u1 - u0);
-  const int t_first = (int)(u0 / S), j_first = (int)(u0 % S);
-  const int Si = (int)S;
-
+  // chain barrier words of the CTA (after every warp's stage barriers)
+  uint32_t* cta_count = reinterpret_cast<uint32_t*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
+  uint32_t* cta_gen = cta_count + 1;
+  const int64_t cta_first = (int64_t)blockIdx.x * kWarps;
+  const uint32_t warps_here = (uint32_t)(wact - cta_first < kWarps ? wact - cta_first : kWarps);
+  const uint32_t ctas = (uint32_t)((wact + kWarps - 1) / kWarps);
+  if (NOPS > 1 && threadIdx.x == 0) {
+    *cta_count = 0u;
+    *cta_gen = 0u;
+  }
+  if (NOPS > 1) __syncthreads();  // every thread of the CTA gets here: inactive warps return below
+  if (wg >= wact) return;
   if (lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+    for (int g = 0; g < p.nops && g < 4; ++g)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.op[g].tmw)) : "memory");
     for (int i = 0; i < NS; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
   __syncwarp();
-  // Weights do not depend on earlier kernels: start streaming them, then wait
-  // for the preceding grid (programmatic dependent launch) before touching
-  // activations, outputs or the split-reduction workspace.
-  int ti = t_first, ji = j_first;  // (tile, span) of the next unit to issue
-  for (int i = 0; i < NS - 1 && i < nunits; ++i) {
-    issue_w<V, MB>(&tmw, M, ti, ji, ring + (size_t)i * SB, smem_addr(&bars[i]), lane);
-    if (++ji == Si) { ji = 0; ++ti; }
-  }
+
+  // cw: next unit whose weights to copy (unit index iw of this warp);
+  // cx: next unit whose activations to copy (ix <= iw); activations of
+  // product g may be read once g <= readable.
+  Cursor cw, cx;
+  cursor_begin(cw, p, 0, wg);
+  cx = cw;
+  int iw = 0, ix = 0, readable = 0;
+  auto issue_w_next = [&]() {
+    const int st = iw % NS;
+    issue_w<V, MB>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
+    const int g0 = cw.g;
+    ++iw;
+    cursor_next(cw, p, wg);
+    if (cw.g != g0 && cw.g < p.nops && lane == 0)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.op[cw.g].tmw)) : "memory");
+  };
+  auto issue_x_ready = [&]() {
+    while (ix < iw && cx.g <= readable) {
+      const int st = ix % NS;
+      issue_x<V, MB>(p.op[cx.g].X, p.op[cx.g].K, M, cx.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
+      ++ix;
+      cursor_next(cx, p, wg);
+    }
+  };
+
+  // Start streaming weights, then wait for the preceding grid before
+  // touching activations, outputs or the split-reduction workspace.
+  while (iw < NS - 1 && cw.g < p.nops) issue_w_next();
   grid_dependency_wait();
   grid_launch_dependents();
   __syncwarp();
-  {
-    int jx = j_first;
-    for (int i = 0; i < NS - 1 && i < nunits; ++i) {
-      issue_x<V, MB>(X, K, M, jx, ring + (size_t)i * SB, smem_addr(&bars[i]), lane);
-      if (++jx == Si) jx = 0;
-    }
-  }
+  issue_x_ready();
 
-  const int q = lane >> 2, c = lane & 3;
-  const bool bcol = q < M;  // this lane holds B column q (activation row q)
-  // Column-split mode (M == 1): B column q = (block of lane c', half hb) is
-  // non-zero only on lanes with q == 2c + hb.
-  constexpr bool COL = MB == 1;
-  const int hb = q & 1;
-  const bool bact = (q >> 1) == c;
-  const uint32_t sel0 = !bact ? 0x4444u : (hb ? 0x1044u : 0x4410u);  // (x[2s], 0) or (0, x[2s+16])
-  const uint32_t sel1 = !bact ? 0x4444u : (hb ? 0x3244u : 0x4432u);  // (x[2s+1], 0) or (0, x[2s+17])
-
-  // acc[mt][r]: m-tile mt, D element r (rows q / q+8, columns 2c / 2c+1)
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-
-  int t = t_first, j = j_first;  // (tile, span) of the unit being computed
-  int js = j_first;              // first span of the current tile segment
-  int i = 0;
+  int i = 0;  // this warp's unit being computed
   bool failed = false;
-  for (; i < nunits; ++i) {
-    const int st = i % NS;
-    if (i + NS - 1 < nunits) {
-      const int sn = (i + NS - 1) % NS;
-      issue_w<V, MB>(&tmw, M, ti, ji, ring + (size_t)sn * SB, smem_addr(&bars[sn]), lane);
+  for (int g = 0; g < p.nops && !failed; ++g) {
+    if (g > 0) {
+      // fill the whole ring with weights of the products ahead, then wait
+      while (iw < i + NS && cw.g < p.nops) issue_w_next();
+      if (!grid_barrier(p.gbar, (uint32_t)g, ctas, warps_here, cta_count, cta_gen, p.err, lane)) {
+        failed = true;
+        break;
+      }
+      readable = g;
+      issue_x_ready();
+    }
+    const StreamOp& op = p.op[g];
+    const int64_t U = op.units, S = op.nspans;
+    if (wg >= op.wact) continue;
+    const int64_t u0 = U * wg / op.wact, u1 = U * (wg + 1) / op.wact;
+    const int nunits = (int)(u1 - u0);
+    const int t_first = (int)(u0 / S), Si = (int)S;
+    int t = t_first, j = (int)(u0 % S), js = j;
+    for (int k = 0; k < nunits; ++k, ++i) {
+      // keep NS - 1 units in flight ahead of the one being computed
+      while (iw < i + NS && cw.g < p.nops) issue_w_next();
       __syncwarp();
-      issue_x<V, MB>(X, K, M, ji, ring + (size_t)sn * SB, smem_addr(&bars[sn]), lane);
-      if (++ji == Si) { ji = 0; ++ti; }
-    }
-    if (!mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / NS) & 1))) {
-      failed = true;
-      break;
-    }
-    const uint8_t* stage = ring + (size_t)st * SB;
-    const uint4* xs = reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + (bcol ? q : 0) * XROW);
-
-    if constexpr (COL) {
-      // M == 1, column split: B column n = 2c' + h holds x only for the k rows
-      // of lane c''s block and half h, so D[row][2c + h] is the half-block sum
-      // sum_i (Codebook10[q_i] / 2) * x_i of lane c's block.  Lane (q, c) thus
-      // holds exactly its own block's half sums for rows q, q+8 (per m-tile),
-      // and applies the scales once per half-block in fp32.
-#pragma unroll
-      for (int phi = 0; phi < F::BPL; ++phi) {
-        // the 16 activations of half hb of the lane's block (zeros if inactive)
-        uint32_t xh[8];
-        if (bact) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint4 v = xs[(c * F::BPL + phi) * 4 + 2 * hb + k];
-            xh[4 * k] = v.x;
-            xh[4 * k + 1] = v.y;
-            xh[4 * k + 2] = v.z;
-            xh[4 * k + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) xh[k] = 0u;
-        }
-        uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
-        const uint8_t* sb = stage + c * F::LANE_BYTES;
-#pragma unroll
-        for (int k = 0; k < SW; ++k) {
-          w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
-          w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
-          w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
-          w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
-        }
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const int pos = phi * F::BB + 2 * s;
-          // (x[2s] or x[2s+16], 0) / (0, ...) as selected for this lane; zeros if inactive
-          const uint32_t b0 = __byte_perm(xh[s], 0u, sel0);
-          const uint32_t b1 = __byte_perm(xh[s], 0u, sel1);
-          uint32_t a[4];
-          a[0] = code_pair<ACT>(e2m1x2_at(w0, pos));
-          a[1] = code_pair<ACT>(e2m1x2_at(w1, pos));
-          a[2] = code_pair<ACT>(e2m1x2_at(w0, pos + 1));
-          a[3] = code_pair<ACT>(e2m1x2_at(w1, pos + 1));
-          mma16816(d0, a, b0, b1, ACT == 1);
-          a[0] = code_pair<ACT>(e2m1x2_at(w2, pos));
-          a[1] = code_pair<ACT>(e2m1x2_at(w3, pos));
-          a[2] = code_pair<ACT>(e2m1x2_at(w2, pos + 1));
-          a[3] = code_pair<ACT>(e2m1x2_at(w3, pos + 1));
-          mma16816(d1, a, b0, b1, ACT == 1);
-        }
-        // E4M3 values of the scales of the lane's block, rows q, q+8, q+16, q+24
-        const float2 e0 = scale_pair_f32<V>(w0, phi), e1 = scale_pair_f32<V>(w1, phi);
-        const float2 e2 = scale_pair_f32<V>(w2, phi), e3 = scale_pair_f32<V>(w3, phi);
-        acc[0][0] = fmaf(d0[0], e0.x, acc[0][0]);
-        acc[0][1] = fmaf(d0[1], e0.y, acc[0][1]);
-        acc[0][2] = fmaf(d0[2], e1.x, acc[0][2]);
-        acc[0][3] = fmaf(d0[3], e1.y, acc[0][3]);
-        acc[1][0] = fmaf(d1[0], e2.x, acc[1][0]);
-        acc[1][1] = fmaf(d1[1], e2.y, acc[1][1]);
-        acc[1][2] = fmaf(d1[2], e3.x, acc[1][2]);
-        acc[1][3] = fmaf(d1[3], e3.y, acc[1][3]);
+      issue_x_ready();
+      const int st = i % NS;
+      if (!mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / NS) & 1))) {
+        failed = true;
+        break;
       }
-    } else {
-      // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or
-      // 32 MMAs) and is then flushed into round-to-nearest fp32 registers.
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int phi = 0; phi < F::BPL; ++phi) {
-        // 32 activations of the lane's block (block c*BPL + phi of the unit)
-        uint32_t xv[16];
-        if (bcol) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
-            xv[4 * k] = v.x;
-            xv[4 * k + 1] = v.y;
-            xv[4 * k + 2] = v.z;
-            xv[4 * k + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) xv[k] = 0u;
-        }
-        // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
-        uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
-        const uint8_t* sb = stage + c * F::LANE_BYTES;
-#pragma unroll
-        for (int k = 0; k < SW; ++k) {
-          w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
-          w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
-          w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
-          w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
-        }
-        const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
-        const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const int pos = phi * F::BB + 2 * s;
-          // B rows (2c, 2c+1) = (x[2s], x[2s+16]); rows (2c+8, 2c+9) = (x[2s+1], x[2s+17]).
-          const uint32_t b0 = __byte_perm(xv[s], xv[8 + s], 0x5410);
-          const uint32_t b1 = __byte_perm(xv[s], xv[8 + s], 0x7632);
-          uint32_t a[4];
-          a[0] = weight_pair<ACT>(e2m1x2_at(w0, pos), s0);
-          a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
-          a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
-          a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
-          mma16816(d0, a, b0, b1, ACT == 1);
-          a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
-          a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
-          a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
-          a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
-          mma16816(d1, a, b0, b1, ACT == 1);
-        }
+      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc);
+      __syncwarp();
+      fence_proxy_async();
+      if (j == Si - 1 || k == nunits - 1) {
+        finish_tile<MB>(p, op, wg, t, t_first, js, j, lane, acc);
+        js = 0;
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        acc[0][r] += d0[r];
-        acc[1][r] += d1[r];
+      if (++j == Si) {
+        j = 0;
+        ++t;
       }
     }
-    __syncwarp();
-    fence_proxy_async();
-
-    if (j == Si - 1 || i == nunits - 1) {
-      // Tile t done for this warp (spans [js, j]).  Bring the partial sums to
-      // lanes: in column-split mode add the two halves and the four lanes of
-      // each quad (fixed order), so lane (q, 0) holds rows q, q+8, q+16, q+24.
-      if constexpr (COL) {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          float ra = acc[mt][0] + acc[mt][1], rb = acc[mt][2] + acc[mt][3];
-          ra += __shfl_xor_sync(0xffffffffu, ra, 1);
-          rb += __shfl_xor_sync(0xffffffffu, rb, 1);
-          ra += __shfl_xor_sync(0xffffffffu, ra, 2);
-          rb += __shfl_xor_sync(0xffffffffu, rb, 2);
-          acc[mt][0] = ra;  // (Codebook10 / 2) x E4M3 = Codebook10 x half-scale
-          acc[mt][2] = rb;
-          acc[mt][1] = acc[mt][3] = 0.f;
-        }
-      }
-      const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
-      const bool owner = !COL || c == 0;  // lanes holding finished values
-      bool store = true;
-      if (!(js == 0 && j == Si - 1)) {
-        float* rec = ws + (2 * wg + (t == t_first ? 0 : 1)) * (kTileRows * 8);
-        if (owner) {
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            const int r0 = mt * 16 + q;
-            rec[r0 * 8 + c0] = acc[mt][0];
-            rec[(r0 + 8) * 8 + c0] = acc[mt][2];
-            if (!COL) {
-              rec[r0 * 8 + c1] = acc[mt][1];
-              rec[(r0 + 8) * 8 + c1] = acc[mt][3];
-            }
-          }
-        }
-        __syncwarp();  // orders the warp's partial stores before lane 0's release
-        const int64_t tS = (int64_t)t * S;
-        const int64_t wf = owner_of(tS, U, wact), wl = owner_of(tS + S - 1, U, wact);
-        uint32_t old = 0;
-        if (lane == 0) old = atomic_add_acq_rel_gpu(&cnt[wf], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
-        store = (int64_t)old == wl - wf;
-        if (store) {
-          // Last contributor: lane r sums row r of the tile over all records
-          // in contributor (= K) order and stores it.  Every contributor after
-          // the first starts inside tile t (record slot 0); the first is in
-          // slot 1 if it started before the tile.
-          const bool first_in_slot1 = U * wf / wact < tS;
-          const int64_t row = (int64_t)t * kTileRows + lane;
-          if (M == 1) {
-            float sum = 0.f;
-            for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
-              float v[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int64_t w2 = w0 + k;
-                const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-                v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8) : 0.f;
-              }
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (w0 + k <= wl) sum += v[k];
-            }
-            if (row < N) Y[row] = sum;
-          } else {
-            // the 8 column slots of row `lane` are 32 contiguous bytes per record
-            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
-              float4 v[4][2];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int64_t w2 = w0 + k;
-                const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-                const float4* r2 = reinterpret_cast<const float4*>(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8);
-                if (w2 <= wl) {
-                  v[k][0] = __ldcg(r2);
-                  v[k][1] = __ldcg(r2 + 1);
-                } else {
-                  v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-              }
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                if (w0 + k <= wl) {
-                  sum[0] += v[k][0].x; sum[1] += v[k][0].y; sum[2] += v[k][0].z; sum[3] += v[k][0].w;
-                  sum[4] += v[k][1].x; sum[5] += v[k][1].y; sum[6] += v[k][1].z; sum[7] += v[k][1].w;
-                }
-            }
-            if (row < N)
-#pragma unroll
-              for (int m = 0; m < 8; ++m)
-                if (m < M) Y[m * N + row] = sum[m];
-          }
-          __syncwarp();
-          if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
-        }
-        store = false;  // the last contributor stored above
-      }
-      if (store && owner) {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
-          if (c0 < M) {
-            if (ra < N) Y[c0 * N + ra] = acc[mt][0];
-            if (rb < N) Y[c0 * N + rb] = acc[mt][2];
-          }
-          if (!COL && c1 < M) {
-            if (ra < N) Y[c1 * N + ra] = acc[mt][1];
-            if (rb < N) Y[c1 * N + rb] = acc[mt][3];
-          }
-        }
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
-      js = 0;
-    }
-    if (++j == Si) { j = 0; ++t; }
   }
 
   if (failed) {
     if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-    // Let every copy already issued land before the shared memory is released.
-    for (int k = i; k < nunits && k < i + NS; ++k)
-      (void)mbar_wait_bounded(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1));
+    // Complete every armed stage (its activation copies too, whatever they
+    // read) and let all copies land before the shared memory is released.
+    readable = p.nops;
+    __syncwarp();
+    issue_x_ready();
+    for (int k = i; k < iw; ++k) (void)mbar_wait_bounded(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1));
+  } else if (p.nops > 1) {
+    // Exit arrival: the CTA's last warp arrives once more on the grid counter
+    // (every CTA arrives nops times in all); the final arrival of the grid
+    // puts the counter back to zero for the next launch.
+    __syncwarp();
+    if (lane == 0) {
+      uint32_t old;
+      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_addr(cta_count)) : "memory");
+      if (old + 1 == (uint32_t)p.nops * warps_here) {
+        const uint32_t g_old = atomicAdd(p.gbar, 1u);
+        if (g_old + 1 == (uint32_t)p.nops * ctas) store_relaxed_gpu(p.gbar, 0u);
+      }
+    }
   }
 }
 
-// Kernel instance for (variant, activation type, staged activation rows).
-template <int V, int ACT>
+// Kernel instance for (variant, activation type, staged activation rows,
+// single product or chain).
+template <int V, int ACT, int NOPS>
 const void* kernel_for_mb(int mb) {
   switch (mb) {
-    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1>);
-    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2>);
-    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4>);
-    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8>);
+    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS>);
+    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS>);
+    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS>);
+    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS>);
   }
 }
 
-const void* stream_kernel(int variant, int act, int mb) {
-  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0>(mb) : kernel_for_mb<0, 1>(mb);
-  return act == 0 ? kernel_for_mb<1, 0>(mb) : kernel_for_mb<1, 1>(mb);
+const void* stream_kernel(int variant, int act, int mb, bool chain) {
+  if (chain) {
+    if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, kChainOps>(mb) : kernel_for_mb<0, 1, kChainOps>(mb);
+    return act == 0 ? kernel_for_mb<1, 0, kChainOps>(mb) : kernel_for_mb<1, 1, kChainOps>(mb);
+  }
+  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, 1>(mb) : kernel_for_mb<0, 1, 1>(mb);
+  return act == 0 ? kernel_for_mb<1, 0, 1>(mb) : kernel_for_mb<1, 1, 1>(mb);
 }
 
 template <int V>
@@ -514,13 +704,25 @@ int stream_weights_per_unit(int variant) { return variant == 0 ? Fmt<0>::KU : Fm
 size_t stream_smem_bytes(int variant, int mb) { return variant == 0 ? smem_for_mb<0>(mb) : smem_for_mb<1>(mb); }
 
 cudaError_t stream_prepare(int variant, int act, int mb) {
-  return cudaFuncSetAttribute(stream_kernel(variant, act, mb), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)stream_smem_bytes(variant, mb));
+  for (int chain = 0; chain < 2; ++chain) {
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel(variant, act, mb, chain != 0),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes(variant, mb));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, stream_kernel(variant, act, mb), kWarps * 32,
-                                                       stream_smem_bytes(variant, mb));
+  // The chain instance must fit as many CTAs per SM (all of its CTAs are co-resident).
+  int one = 0, chain = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&one, stream_kernel(variant, act, mb, false), kWarps * 32,
+                                                                stream_smem_bytes(variant, mb));
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&chain, stream_kernel(variant, act, mb, true), kWarps * 32,
+                                                    stream_smem_bytes(variant, mb));
+  if (e != cudaSuccess) return e;
+  *ctas_per_sm = one < chain ? one : chain;
+  return cudaSuccess;
 }
 
 namespace {
@@ -538,36 +740,92 @@ cudaError_t stream_init_driver() {
   return cudaSuccess;
 }
 
-cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s) {
-  if (!g_encode) return cudaErrorInitializationError;
-  const int mb = stream_mb_for(a.M);
-  const size_t smem = stream_smem_bytes(variant, mb);
+namespace {
+
+cudaError_t encode_weights(int variant, const GemvArgs& a, CUtensorMap* tmw) {
   const int span = variant == 0 ? Fmt<0>::SPAN : Fmt<1>::SPAN;
   // Weights as a 2-D array of 32-bit words: row_bytes/4 columns, N rows.
-  CUtensorMap tmw;
   cuuint64_t dims[2] = {(cuuint64_t)(a.row_bytes / 4), (cuuint64_t)a.N};
   cuuint64_t strides[1] = {(cuuint64_t)a.row_bytes};
   cuuint32_t box[2] = {(cuuint32_t)(span / 4), (cuuint32_t)kTileRows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.W), dims, strides, box, estr,
+  CUresult r = g_encode(tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.W), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int NOPS>
+cudaError_t fill_params(int variant, const GemvArgs* ops, int nops, uint32_t* gbar, StreamParams<NOPS>* p) {
+  memset(p, 0, sizeof(*p));
+  for (int g = 0; g < nops; ++g) {
+    cudaError_t e = encode_weights(variant, ops[g], &p->op[g].tmw);
+    if (e != cudaSuccess) return e;
+    p->op[g].X = ops[g].X;
+    p->op[g].Y = ops[g].Y;
+    p->op[g].N = ops[g].N;
+    p->op[g].K = ops[g].K;
+    p->op[g].units = ops[g].units;
+    p->op[g].nspans = ops[g].nspans;
+    p->op[g].wact = ops[g].units < ops[g].wact ? ops[g].units : ops[g].wact;
+  }
+  p->ws = ops[0].ws;
+  p->cnt = ops[0].cnt;
+  p->err = ops[0].err;
+  p->gbar = gbar;
+  p->wact = 0;
+  for (int g = 0; g < nops; ++g) p->wact = ops[g].wact > p->wact ? ops[g].wact : p->wact;
+  p->nops = nops;
+  p->M = ops[0].M;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s) {
+  if (!g_encode) return cudaErrorInitializationError;
+  const int mb = stream_mb_for(a.M);
+  StreamParams<1> p;
+  cudaError_t e = fill_params(variant, &a, 1, nullptr, &p);
+  if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the kernel may start (and stream weights)
   // while the previous kernel on the stream drains; it calls
   // griddepcontrol.wait before reading anything an earlier kernel writes.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {const_cast<GemvArgs*>(&a), &tmw};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb), args);
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, false), args);
+}
+
+cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
+                              cudaStream_t s) {
+  if (!g_encode) return cudaErrorInitializationError;
+  if (nops < 1 || nops > kChainOps) return cudaErrorInvalidValue;
+  const int mb = stream_mb_for(ops[0].M);
+  static thread_local StreamParams<kChainOps> p;  // 9 KB: kept off the stack
+  cudaError_t e = fill_params(variant, ops, nops, gbar, &p);
+  if (e != cudaSuccess) return e;
+  // Cooperative: every CTA is resident at once, as the grid barriers need.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, true), args);
 }
 
 }  // namespace rocmfp4

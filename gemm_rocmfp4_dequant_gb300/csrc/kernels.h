@@ -34,6 +34,12 @@ cudaError_t stream_prepare(int variant, int act, int mb);  // sets the dynamic s
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm);
 cudaError_t stream_init_driver();           // resolves cuTensorMapEncodeTiled once
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s);
+// Up to kChainOps products with the same variant, activation type, M and
+// wact, in order, in one cooperative launch with a grid barrier after each
+// product (gbar: a zeroed counter).
+constexpr int kChainOps = 48;
+cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
+                              cudaStream_t s);
 
 // Tensor-core product Y[M][N] = X[M][K] . W[N][K]^T (tcgen05, decoded weights
 // in tensor memory).  Needs K % tc_k_multiple(variant) == 0, W and X 16-byte

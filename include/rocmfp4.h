@@ -109,6 +109,38 @@ rocmfp4_status rocmfp4_gemm_ex(const void *W, const void *X, float *Y, int64_t M
                                int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                rocmfp4_stream_t stream);
 
+/* One product of a chain: Y = X . W^T with the layouts of rocmfp4_gemm_ex
+ * (X is M x K of the chain's activation type, Y is M x N fp32). */
+typedef struct rocmfp4_gemv_op {
+  const void *W;
+  const void *X;
+  float *Y;
+  int64_t N;
+  int64_t K;
+} rocmfp4_gemv_op;
+
+/* Runs the products ops[0 .. count-1] in order on one stream, all with the
+ * same M, variant and activation type: the result is that of calling
+ * rocmfp4_gemm_ex for each in turn, and product i may read (through X)
+ * memory that products 0 .. i-1 write.
+ *
+ * This is the decode-step form: for M <= 8, consecutive products whose K is
+ * a multiple of 256 (dual) or 512 (single-scale) and whose W and X are
+ * 16-byte aligned run in one cooperative launch of the streaming kernel per
+ * group of up to 48, with a grid-wide barrier after each product.  Weights
+ * never depend on earlier products, so the next product's weights stream
+ * while the previous one finishes; its activations are read only after the
+ * barrier.  Other products (and every product when M > 8) are launched one
+ * by one.
+ *   - ops is host memory read during the call; count == 0 does nothing.
+ *   - Y of a product must not overlap any W, nor the X or Y of another
+ *     product of the chain, except that X of a later product may be (part
+ *     of) Y of an earlier one.
+ *   - Errors as rocmfp4_gemm_ex, checked for every product before any
+ *     launch; a launch error leaves the products before it done. */
+rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op *ops, int count, int64_t M,
+                                  rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream);
+
 /* Y = X . W^T for M <= 8 without allocating device memory.
  *
  * For callers that cannot call cudaMalloc where they run the product: an
