@@ -3,17 +3,24 @@
 Default workload ("layer"): one dense decoder layer's four dual-scale ROCmFP4
 matrices -- [N, K] = [7168, 5120] (fused QKV), [5120, 6144] (O), [34816, 5120]
 (fused gate+up), [5120, 17408] (down) -- each multiplied by a batch-1 fp16
-activation vector ~ N(0, 1).  One step = the four GEMVs.  Steps rotate over
-enough resident copies of the layer that the working set is far larger than
-L2, so every step streams its weights from HBM.
+activation vector ~ N(0, 1).  One step = the four GEMVs, one launch each,
+replayed as a CUDA graph (programmatic dependent launch between them).  Steps
+rotate over enough resident copies of the layer that the working set is far
+larger than L2, so every step streams its weights from HBM.
 
 Metric: weight-streaming GB/s = (packed weight bytes + activation bytes +
-output bytes) per step / step time, with the roofline of the dominant kernel
-against the measured HBM copy bandwidth.
+output bytes) per step / step time.  The roofline object is that of the
+dominant kernel (the streaming GEMV) against the measured HBM copy bandwidth.
+The same line carries the W4A16 prefill GEMM ("prefill": X bf16 [M, K],
+M in {512, 4096, 23552}, over the four layer shapes) in TFLOP/s against the
+measured bf16 tensor peak.
 
-Other workloads (--workload): single (N=256, K=1024), sweep (both layouts x
-M in {1,2,4,8}), model (64 layers x 4 matrices + LM head [152064, 5120], one
-CUDA graph per token), prefill (M in {512, 4096, 23552}).
+Other workloads (--workload):
+  single   N=256, K=1024 dual GEMV (latency; L2 flushed between iterations)
+  sweep    the four shapes x {dual, single-scale} x M in {1, 2, 4, 8}
+  model    64 layers x the four matrices + LM head [152064, 5120] (12.5 GB),
+           one CUDA graph of 257 GEMVs per token
+  prefill  the prefill GEMM alone
 
 --impl reference times the CPU oracle (the fp64 C implementation under
 oracle/) on the host cores over a bounded sample of the same workload.
@@ -21,8 +28,11 @@ oracle/) on the host cores over a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -36,85 +46,179 @@ sys.path.insert(0, ROOT)
 LAYER = [("qkv", 7168, 5120), ("o", 5120, 6144), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
 LM_HEAD = ("lm_head", 152064, 5120)
 N_LAYERS = 64
+PREFILL_M = (512, 4096, 23552)
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "ROCmFP4 GEMV weight GB/s (% of HBM peak); W4A16 GEMM TFLOP/s (% peak)"
+DATA = "synthetic (seeded SplitMix64 weight bytes, Box-Muller N(0,1) activations)"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_stream_layer_dual_m1.md")
+GEMV_SOURCE = os.path.join(ROOT, "gemm_rocmfp4_dequant_gb300", "csrc", "gemv.cu")
 
 
 def peaks():
+    """(HBM GB/s, bf16 TF/s burst, bf16 TF/s sustained, 'measured' | 'fallback')."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def block_bytes(variant):
+    return 18 if variant == 0 else 17
+
+
+def matrix_bytes(N, K, variant=0):
+    return N * (K // 32) * block_bytes(variant)
+
+
 def step_bytes(mats, variant=0, M=1):
-    bb = 18 if variant == 0 else 17
-    return sum(N * (K // 32) * bb + 2 * M * K + 4 * M * N for _, N, K in mats)
+    """Algorithmic bytes of one pass: packed weights + activations (2 B) + outputs (4 B)."""
+    return sum(matrix_bytes(N, K, variant) + 2 * M * K + 4 * M * N for _, N, K in mats)
 
 
 def weight_bytes(mats, variant=0):
-    bb = 18 if variant == 0 else 17
-    return sum(N * (K // 32) * bb for _, N, K in mats)
+    return sum(matrix_bytes(N, K, variant) for _, N, K in mats)
+
+
+def gemv_traffic():
+    """DRAM bytes per launch of the streaming GEMV on the layer shapes, from the
+    committed ncu summary, if that capture was taken on the current kernel source
+    (its sha256 is recorded in the summary); else None."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+        src = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"dram_bytes_per_launch:\s*(.+)", text)
+    if not m or not t or m.group(1) != src:
+        return None
+    out = {}
+    for part in t.group(1).split(","):
+        k, v = part.strip().split("=")
+        out[k.strip()] = int(v)
+    return out
 
 
 # ---- clocks -------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock and throttle reasons sampled during the timed region: NVML through
+    ctypes every 2 ms (so short regions still get samples), else nvidia-smi every
+    200 ms."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines: list[str] = []
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.samples: list[tuple[float, int]] = []
+        self.max_mhz = None
+        self.kind = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = None
+        self._proc = None
+
+    def _open_nvml(self):
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return False
+        props = torch.cuda.get_device_properties(self.device)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self._reasons_fn = None
+        for name in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            try:
+                self._reasons_fn = getattr(lib, name)
+                break
+            except AttributeError:
+                continue
+        self._nvml, self._handle = lib, h
+        return True
+
+    def _sample_nvml(self):
+        lib, h = self._nvml, self._handle
+        clk, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        while True:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = 0
+                if self._reasons_fn is not None and self._reasons_fn(h, ctypes.byref(reasons)) == 0:
+                    r = reasons.value
+                self.samples.append((float(clk.value), int(r)))
+            if self._stop.wait(0.002):
+                break
+
+    def _read_smi(self):
+        for ln in self._proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            self.max_mhz = mx
+            bits = 0
+            for bit, v in zip((0x8, 0x40, 0x20, 0x4), parts[2:6]):
+                if v.lower() == "active":
+                    bits |= bit
+            self.samples.append((sm, bits))
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+            ok = self._open_nvml()
+        except Exception:
+            ok = False
+        if ok:
+            self.kind = "nvml"
+            self._t = threading.Thread(target=self._sample_nvml, daemon=True)
+            self._t.start()
+            return self
+        try:
+            fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_power_cap")
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device}", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
+            self.kind = "nvidia-smi"
+            self._t = threading.Thread(target=self._read_smi, daemon=True)
             self._t.start()
         except Exception:
-            self.proc = None
+            self.kind = None
         return self
 
-    def _read(self):
-        for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
-
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                self._proc.kill()
+        if self.kind == "nvml":
+            self._t.join(timeout=1)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for name, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": self.kind}
+        sm = [s for s, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(name for bit, name in self.REASONS.items() if bits & bit)
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "source": self.kind}
 
 
 # ---- distributed plumbing (replicas only) -----------------------------------------------
@@ -152,12 +256,11 @@ def max_over_ranks(value: float, world: int) -> float:
 
 # ---- CPU oracle baseline ------------------------------------------------------------------
 
-def cpu_oracle_rate(mats, variant, M, budget_s=12.0, act=0):
-    """Times the oracle on row samples of each matrix; returns (GB/s of the metric, cores, sample text, seconds).
-
-    The sample size is chosen from a short probe so that the timed run takes
-    about budget_s seconds; the metric counts the sampled rows' packed bytes
-    plus their share of activation and output bytes."""
+def cpu_oracle_rate(mats, variant=0, M=1, budget_s=12.0, act=0, rows=None):
+    """Times the oracle on row samples of each matrix; returns (GB/s of the metric,
+    cores, sample text, seconds).  The sample size comes from a short probe so that
+    the timed run takes about budget_s seconds; the metric counts the sampled rows'
+    packed bytes plus their share of activation and output bytes."""
     import oracle
     import synth
     cores = os.cpu_count() or 1
@@ -165,33 +268,113 @@ def cpu_oracle_rate(mats, variant, M, budget_s=12.0, act=0):
     for idx, (name, N, K) in enumerate(mats):
         inputs.append((N, K, synth.activations(M, K, act, seed=0, stream=synth.act_stream(0, idx))))
 
-    def run(rows_per):
+    cache = {}
+
+    def run(rows_per, passes=1):
         nbytes, secs = 0.0, 0.0
         for idx, (N, K, Xh) in enumerate(inputs):
-            rows = np.arange(min(rows_per, N))
-            Wr = synth.weights(N, K, variant, seed=0, stream=synth.weight_stream(0, idx), rows=rows)
-            t0 = time.perf_counter()
-            oracle.gemm(Wr, Xh, len(rows), K, variant, act=act, nthreads=cores)
-            secs += time.perf_counter() - t0
-            rb = (K // 32) * (18 if variant == 0 else 17)
-            nbytes += len(rows) * (rb + 4 * M) + 2 * M * K * len(rows) / N
+            n = min(rows_per, N)
+            if (idx, n) not in cache:
+                cache[(idx, n)] = synth.weights(N, K, variant, seed=0, stream=synth.weight_stream(0, idx),
+                                                rows=np.arange(n))
+            Wr = cache[(idx, n)]
+            for _ in range(passes):
+                t0 = time.perf_counter()
+                oracle.gemm(Wr, Xh, n, K, variant, act=act, nthreads=cores)
+                secs += time.perf_counter() - t0
+                rb = (K // 32) * block_bytes(variant)
+                nbytes += n * (rb + 4 * M) + 2 * M * K * n / N
         return nbytes, secs
 
-    probe_rows = 2 * cores
-    b, t = run(probe_rows)
-    rows_per = int(max(probe_rows, min(min(N for _, N, _ in mats), probe_rows * budget_s / max(t, 1e-3))))
-    b, t = run(rows_per)
-    desc = (f"{rows_per} rows of each of the {len(mats)} matrices (M={M}), "
-            f"oracle threaded over rows on {cores} cores")
+    passes = 1
+    if rows is None:
+        # grow a probe until it takes a quarter of the budget (small probes are
+        # dominated by fixed costs), then scale to the budget
+        nmax = max(N for _, N, _ in mats)
+        rows = 2 * cores
+        b, t = run(rows)
+        while t < budget_s / 4 and rows < nmax:
+            rows = min(nmax, rows * 4)
+            b, t = run(rows)
+        if rows < nmax:
+            rows = int(min(nmax, rows * budget_s / max(t, 1e-3)))
+        else:  # whole matrices are quicker than the budget: repeat them
+            passes = max(1, int(budget_s / max(t, 1e-3)))
+    rows_per = rows
+    b, t = run(rows_per, passes)
+    desc = (f"{passes} pass(es) over {rows_per if rows_per < max(N for _, N, _ in mats) else 'all'} rows of each of "
+            f"the {len(mats)} matrices (M={M}), oracle threaded over rows on {cores} cores")
     return b / t / 1e9, cores, desc, t
 
 
-# ---- GPU workloads -----------------------------------------------------------------------------
+def cpu_oracle_flops(mats, M, budget_s=8.0, act=1, rows=None):
+    """Oracle TFLOP/s of the prefill product on a sample of rows x tokens."""
+    import oracle
+    import synth
+    cores = os.cpu_count() or 1
+    toks = min(M, 64)
 
-class LayerStep:
-    """R resident copies of one layer (four matrices); step i runs the four GEMVs of copy i % R."""
+    def run(rows_per):
+        flops, secs = 0.0, 0.0
+        for idx, (name, N, K) in enumerate(mats):
+            rows = np.arange(min(rows_per, N))
+            Wr = synth.weights(N, K, 0, seed=0, stream=synth.weight_stream(0, idx), rows=rows)
+            Xh = synth.activations(toks, K, act, seed=0, stream=synth.act_stream(0, idx))
+            t0 = time.perf_counter()
+            oracle.gemm(Wr, Xh, len(rows), K, 0, act=act, nthreads=cores)
+            secs += time.perf_counter() - t0
+            flops += 2.0 * toks * len(rows) * K
+        return flops, secs
 
-    def __init__(self, mats, variant, M, act, copies):
+    if rows is None:
+        f, t = run(cores)
+        rows = int(max(cores, min(5120, cores * budget_s / max(t, 1e-3))))
+    rows_per = rows
+    f, t = run(rows_per)
+    return f / t / 1e12, cores, f"{rows_per} rows x {toks} tokens of each layer matrix, {cores} cores", t
+
+
+# ---- timing helpers ---------------------------------------------------------------------------
+
+def time_steps(step_fn, steps, warmup, world):
+    """Seconds for `steps` calls of step_fn after `warmup`, between CUDA events on the
+    current stream, with a device synchronisation and a barrier on both sides."""
+    import torch
+    for i in range(warmup):
+        step_fn(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for i in range(steps):
+        step_fn(warmup + i)
+    b.record(s)
+    b.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    return a.elapsed_time(b) / 1e3
+
+
+class L2Flush:
+    """A buffer larger than L2; writing it evicts whatever an earlier call left in L2."""
+
+    def __init__(self):
+        import torch
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+# ---- batch-1 / small-batch GEMV workloads ---------------------------------------------------
+
+class GemvStep:
+    """R resident copies of a list of matrices; step i runs one product per matrix
+    of copy i % R (one launch each), captured per copy as a CUDA graph."""
+
+    def __init__(self, mats, variant, M, act, copies, seed0=0):
         import torch
 
         import gemm_rocmfp4_dequant_gb300 as rf4
@@ -204,9 +387,9 @@ class LayerStep:
             Wc, Xc, Yc = [], [], []
             for m, (name, N, K) in enumerate(mats):
                 w = torch.empty(N * rf4.row_bytes(K, variant), dtype=torch.uint8, device="cuda")
-                synth.device.fill_weights(w, N, K, variant, seed=r, stream=synth.weight_stream(0, m))
+                synth.device.fill_weights(w, N, K, variant, seed=seed0 + r, stream=synth.weight_stream(m // 5, m % 5))
                 x = torch.empty((M, K), dtype=torch.int16, device="cuda")
-                synth.device.fill_act(x, act, seed=r, stream=synth.act_stream(0, m))
+                synth.device.fill_act(x, act, seed=seed0 + r, stream=synth.act_stream(m // 5, m % 5))
                 Wc.append(w)
                 Xc.append(x.view(dt))
                 Yc.append(torch.empty((M, N), dtype=torch.float32, device="cuda"))
@@ -226,7 +409,7 @@ class LayerStep:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.run(0, s)  # first call on the device does the library's one-time set-up
+            self.run(0, s)  # the first call on the device does the library's one-time set-up
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         self.graphs = []
@@ -238,28 +421,15 @@ class LayerStep:
         torch.cuda.synchronize()
 
     def launches_per_step(self):
-        return len(self.mats) * ((self.M + 7) // 8)
+        return len(self.mats)
 
 
-def time_steps(step_fn, steps, warmup, world):
-    import torch
-    for i in range(warmup):
-        step_fn(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for i in range(steps):
-        step_fn(warmup + i)
-    b.record()
-    b.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    return a.elapsed_time(b) / 1e3
+def copies_for(mats, variant):
+    """Resident copies so that a rotation streams more than four times the L2."""
+    return max(2, int(np.ceil(4 * L2_BYTES / weight_bytes(mats, variant))) + 1)
 
 
-def per_matrix_kernel_times(L: LayerStep, reps=None):
+def per_matrix_kernel_times(L: GemvStep, reps=None):
     """Average device time of each matrix's kernel: a CUDA graph of `reps` launches
     of that matrix's product (rotating over the resident copies, so every launch
     streams from HBM) is replayed between CUDA events on the launching stream."""
@@ -274,8 +444,8 @@ def per_matrix_kernel_times(L: LayerStep, reps=None):
                 L.rf4.gemm(L.W[r][m], L.X[r][m], N, K, L.variant, Y=L.Y[r][m])
         g.replay()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         for _ in range(3):
             g.replay()
@@ -286,10 +456,10 @@ def per_matrix_kernel_times(L: LayerStep, reps=None):
     return out
 
 
-def e2e_rate(L: LayerStep, steps, warmup, world):
-    """Same metric through the public API with host buffers: each step copies the four
-    activation vectors from pinned host memory, runs the four products and reads the
-    four outputs back into pinned host memory; weights stay resident."""
+def e2e_rate(L: GemvStep, steps, warmup, world):
+    """The metric through the public API with host buffers: every step copies each
+    matrix's activations from pinned host memory, runs the products and reads every
+    output back into pinned host memory; weights stay resident."""
     import torch
     hx = [[x.cpu().pin_memory() for x in Xc] for Xc in L.X]
     hy = [[torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in Yc] for Yc in L.Y]
@@ -309,96 +479,327 @@ def e2e_rate(L: LayerStep, steps, warmup, world):
     return t, h2d, d2h
 
 
-def run_layer(args, world, rank, hbm, mats=None, variant=0, M=1, act=0, label="layer"):
+def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True):
+    """Timed steps of the GEMV workload; returns the measurements of the JSON line."""
     import torch
-    mats = mats or LAYER
-    per_copy = weight_bytes(mats, variant)
-    copies = max(2, int(np.ceil(4 * L2_BYTES / per_copy)) + 1)
-    L = LayerStep(mats, variant, M, act, copies)
+    copies = copies_for(mats, variant)
+    L = GemvStep(mats, variant, M, act, copies)
     L.capture()
     launches0 = L.rf4.launch_count()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t = time_steps(lambda i: L.graphs[i % copies].replay(), args.steps, args.warmup, world)
     t = max_over_ranks(t, world)
     sb = step_bytes(mats, variant, M)
-    value = world * sb * args.steps / t / 1e9
     kt = per_matrix_kernel_times(L)
-    algo = [N * (K // 32) * (18 if variant == 0 else 17) + 2 * M * K + 4 * M * N for _, N, K in mats]
+    algo = [matrix_bytes(N, K, variant) + 2 * M * K + 4 * M * N for _, N, K in mats]
     achieved = sum(algo) / sum(kt) / 1e9
-    te, h2d, d2h = e2e_rate(L, max(10, args.steps // 4), args.warmup, world)
-    te = max_over_ranks(te, world)
-    e2e = world * sb * max(10, args.steps // 4) / te / 1e9
     res = dict(
-        value=value, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
-        gpu_launches=L.launches_per_step() * args.steps,
-        graph_launches_check=L.rf4.launch_count() - launches0,
-        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                  "frac": round(achieved / hbm, 4), "traffic": None,
-                  "per_launch_us": {n: round(x * 1e6, 2) for (n, _, _), x in zip(mats, kt)}},
-        e2e={"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        copies=copies, footprint_gb=round(copies * per_copy / 1e9, 3),
-    )
+        value=world * sb * args.steps / t / 1e9, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
+        gpu_launches=L.launches_per_step() * args.steps, copies=copies,
+        footprint_gb=round(copies * weight_bytes(mats, variant) / 1e9, 3),
+        per_launch_us={n: round(x * 1e6, 2) for (n, _, _), x in zip(mats, kt)},
+        achieved=achieved, algo_bytes={n: a for (n, _, _), a in zip(mats, algo)}, kernel_s=kt,
+        graph_launch_check=L.rf4.launch_count() - launches0)
+    if with_e2e:
+        ne = max(10, args.steps // 4)
+        te, h2d, d2h = e2e_rate(L, ne, args.warmup, world)
+        te = max_over_ranks(te, world)
+        res["e2e"] = {"value": round(world * sb * ne / te / 1e9, 1), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del L
+    torch.cuda.empty_cache()
     return res
+
+
+# ---- prefill GEMM ---------------------------------------------------------------------------
+
+def run_prefill(Ms, tflops_peak, reps_small=10, reps_large=3):
+    """W4A16 prefill GEMM (dual weights, X bf16 [M, K] ~ N(0,1), Y fp32) over the four
+    layer shapes for each M: every call is timed alone between CUDA events, with L2
+    flushed before it (outside the events).  Returns per-M totals and per-shape times."""
+    import torch
+
+    import gemm_rocmfp4_dequant_gb300 as rf4
+    import synth.device
+    flush = L2Flush()
+    out = {}
+    launches = 0
+    for M in Ms:
+        tot_f, tot_t, shapes = 0.0, 0.0, {}
+        for m, (name, N, K) in enumerate(LAYER):
+            W = torch.empty(N * rf4.row_bytes(K, 0), dtype=torch.uint8, device="cuda")
+            synth.device.fill_weights(W, N, K, 0, seed=0, stream=synth.weight_stream(0, m))
+            X = torch.empty((M, K), dtype=torch.int16, device="cuda")
+            synth.device.fill_act(X, 1, seed=0, stream=synth.act_stream(0, m))
+            X = X.view(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            for _ in range(2):
+                rf4.gemm(W, X, N, K, 0, Y=Y)
+            reps = reps_small if M <= 4096 else reps_large
+            s = torch.cuda.current_stream()
+            times = []
+            for _ in range(reps):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                rf4.gemm(W, X, N, K, 0, Y=Y)
+                b.record(s)
+                b.synchronize()
+                times.append(a.elapsed_time(b) / 1e3)
+            launches += reps + 2
+            t = float(np.median(times))
+            f = 2.0 * M * N * K
+            shapes[name] = {"us": round(t * 1e6, 1), "tflops": round(f / t / 1e12, 1)}
+            tot_f += f
+            tot_t += t
+            del W, X, Y
+            torch.cuda.empty_cache()
+        out[M] = {"tflops": round(tot_f / tot_t / 1e12, 1), "frac": round(tot_f / tot_t / 1e12 / tflops_peak, 4),
+                  "layer_ms": round(tot_t * 1e3, 3), "per_shape": shapes}
+    del flush
+    torch.cuda.empty_cache()
+    return out, launches
+
+
+# ---- single GEMV latency (N=256, K=1024) ------------------------------------------------------
+
+def run_single(args, world):
+    import torch
+
+    import gemm_rocmfp4_dequant_gb300 as rf4
+    import synth.device
+    N, K = 256, 1024
+    W = torch.empty(N * rf4.row_bytes(K, 0), dtype=torch.uint8, device="cuda")
+    synth.device.fill_weights(W, N, K, 0, seed=0, stream=0)
+    x = torch.empty((1, K), dtype=torch.int16, device="cuda")
+    synth.device.fill_act(x, 0, seed=0, stream=synth.act_stream(0, 0))
+    x = x.view(torch.float16)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    flush = L2Flush()
+    for _ in range(args.warmup):
+        rf4.gemm(W, x, N, K, 0, Y=y)
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.current_stream()
+    times = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            rf4.gemm(W, x, N, K, 0, Y=y)
+            b.record(s)
+            b.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+    t = max_over_ranks(float(np.sum(times)), world)
+    sb = step_bytes([("single", N, K)])
+    return dict(value=world * sb * args.steps / t / 1e9, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
+                us_median=round(float(np.median(times)) * 1e6, 2), gpu_launches=args.steps, step_bytes=sb)
+
+
+# ---- whole-model decode step (config: 64 layers x 4 matrices + LM head) --------------------------
+
+class ModelStep:
+    """All weights resident (12.5 GB dual); one CUDA graph of 257 GEMV launches per
+    token, each with its own activation vector (outputs are not chained)."""
+
+    def __init__(self, variant=0):
+        import torch
+
+        import gemm_rocmfp4_dequant_gb300 as rf4
+        import synth
+        import synth.device
+        self.rf4, self.variant = rf4, variant
+        self.mats = [(f"l{l}.{n}", N, K) for l in range(N_LAYERS) for (n, N, K) in LAYER] + [LM_HEAD]
+        self.W, self.X, self.Y = [], [], []
+        for i, (name, N, K) in enumerate(self.mats):
+            layer, m = (i // 4, i % 4) if i < 4 * N_LAYERS else (N_LAYERS, 4)
+            w = torch.empty(N * rf4.row_bytes(K, variant), dtype=torch.uint8, device="cuda")
+            synth.device.fill_weights(w, N, K, variant, seed=0, stream=synth.weight_stream(layer, m))
+            x = torch.empty((1, K), dtype=torch.int16, device="cuda")
+            synth.device.fill_act(x, 0, seed=0, stream=synth.act_stream(layer, m))
+            self.W.append(w)
+            self.X.append(x.view(torch.float16))
+            self.Y.append(torch.empty((1, N), dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run()
+        torch.cuda.synchronize()
+
+    def run(self):
+        for (name, N, K), w, x, y in zip(self.mats, self.W, self.X, self.Y):
+            self.rf4.gemm(w, x, N, K, self.variant, Y=y)
+
+
+def run_model(args, world):
+    import torch
+    S = ModelStep()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t = time_steps(lambda i: S.graph.replay(), args.steps, args.warmup, world)
+    t = max_over_ranks(t, world)
+    sb = step_bytes(S.mats)
+    res = dict(value=world * sb * args.steps / t / 1e9, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
+               tok_s=world * args.steps / t, gpu_launches=len(S.mats) * args.steps, step_bytes=sb,
+               weight_gb=round(weight_bytes(S.mats) / 1e9, 3))
+    del S
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---- main -----------------------------------------------------------------------------------
+
+def base_line(args, world, value, unit, ms, cfg, dtype, higher=True):
+    return {"metric": METRIC, "value": round(value, 4 if value < 10 else 1), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": higher,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": DATA, "config": cfg,
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def reference_line(args, cfg):
+    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    t0 = time.perf_counter()
+    # one probe sizes the sample so that all steps together take about 150 s
+    per_step = 150.0 / (args.steps + args.warmup)
+    cores = os.cpu_count() or 1
+    if args.workload == "prefill":
+        fn = lambda rows=None, b=1.0: cpu_oracle_flops(LAYER, 4096, budget_s=b, rows=rows)
+    elif args.workload == "single":
+        fn = lambda rows=None, b=1.0: cpu_oracle_rate([("single", 256, 1024)], budget_s=b, rows=rows)
+    else:
+        fn = lambda rows=None, b=1.0: cpu_oracle_rate(LAYER, budget_s=b, rows=rows)
+    _, _, _, tp = fn(rows=cores)
+    rows = max(1, int(cores * per_step / max(tp, 1e-4)))
+    vals, desc = [], ""
+    for _ in range(args.warmup + args.steps):
+        v, cores, desc, _ = fn(rows=rows)
+        vals.append(v)
+    v = float(np.mean(vals[args.warmup:]))
+    unit = "TFLOP/s" if args.workload == "prefill" else "GB/s"
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": DATA, "config": dict(cfg, l2="host run"),
+            "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t0, 1)}
+    if unit == "GB/s":
+        sb = step_bytes(LAYER if args.workload != "single" else [("single", 256, 1024)])
+        line["ms_per_step"] = round(sb / (v * 1e9) * 1e3, 3)
+    return line
+
+
+def gemv_roofline(res, hbm, peak_kind, mats, variant, M):
+    traffic = gemv_traffic() if (mats == LAYER and variant == 0 and M == 1) else None
+    roof = {"bound": "hbm", "achieved": round(res["achieved"], 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(res["achieved"] / hbm, 4), "traffic": None,
+            "kernel": "gemv_stream_kernel", "peak_kind": peak_kind, "frac_of": f"{peak_kind} HBM copy bandwidth",
+            "per_launch_us": res["per_launch_us"],
+            "algorithmic_bytes_per_launch": res["algo_bytes"]}
+    if traffic and all(n in traffic for n, _, _ in mats):
+        roof["traffic"] = int(round(sum(traffic[n] for n, _, _ in mats) / len(mats)))
+        roof["traffic_per_launch"] = {n: traffic[n] for n, _, _ in mats}
+        roof["traffic_note"] = "mean DRAM read+write bytes per launch over the four matrices (ncu)"
+    return roof
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="layer", choices=["layer"])
+    ap.add_argument("--workload", default="layer", choices=["layer", "single", "sweep", "model", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="leave the prefill object out of the layer line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     hbm, bf16, bf16_s, peak_kind = peaks()
-    mats = LAYER
-    cfg = {"workload": "layer: batch-1 dual-scale GEMV over [7168,5120] [5120,6144] [34816,5120] [5120,17408], "
-                       "fp16 x ~ N(0,1)", "variant": "dual", "M": 1, "act": "fp16"}
+    cfgs = {
+        "layer": {"workload": "layer sweep: batch-1 dual-scale GEMV, [N,K] = [7168,5120] [5120,6144] "
+                              "[34816,5120] [5120,17408], x fp16 ~ N(0,1), one launch per matrix",
+                  "variant": "dual", "M": 1, "act": "fp16"},
+        "single": {"workload": "single dual-scale GEMV N=256 K=1024, x fp16 ~ N(0,1)", "variant": "dual", "M": 1,
+                   "act": "fp16", "l2": "flushed (256 MB write) before every timed call"},
+        "sweep": {"workload": "the four layer shapes x {dual, single-scale} x M in {1,2,4,8}, x fp16",
+                  "act": "fp16"},
+        "model": {"workload": "whole-model decode step: 64 layers x 4 matrices + LM head [152064,5120], dual, "
+                              "batch 1, fresh x fp16 per GEMV, one CUDA graph of 257 launches per token",
+                  "variant": "dual", "M": 1, "act": "fp16", "l2": "12.5 GB of weights per step > L2"},
+        "prefill": {"workload": "W4A16 prefill GEMM, dual weights of the four layer shapes x X bf16 [M,K] ~ N(0,1), "
+                                "M in {512, 4096, 23552}", "act": "bf16",
+                    "l2": "flushed (256 MB write) before every timed call"},
+    }
+    cfg = cfgs[args.workload]
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        t0 = time.perf_counter()
-        vals = []
-        for _ in range(args.warmup + args.steps):
-            v, cores, desc, _ = cpu_oracle_rate(mats, 0, 1, budget_s=min(10.0, 120.0 / (args.steps + args.warmup)))
-            vals.append(v)
-        v = float(np.mean(vals[args.warmup:]))
-        sb = step_bytes(mats)
-        line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sb / (v * 1e9) * 1e3, 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded SplitMix64 weights, Box-Muller activations)",
-                "config": dict(cfg, l2="CPU run; no GPU L2"),
-                "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                 "sample": desc},
-                "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-                "wall_s": round(time.perf_counter() - t0, 1)}
-        print(json.dumps(line))
+        if rank == 0:
+            print(json.dumps(reference_line(args, cfg)))
         return
 
     import torch
+
     import __graft_entry__
     if rank == 0:
         __graft_entry__.build()
     barrier(world)
-    res = run_layer(args, world, rank, hbm)
-    cfg["l2"] = (f"rotating {res['copies']} resident layer copies ({res['footprint_gb']} GB > 129 MB L2); "
-                 "inputs larger than L2")
-    line = {"metric": METRIC, "value": round(res["value"], 1), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x e2m1 -> f32",
-            "data": "synthetic (seeded SplitMix64 weights, Box-Muller activations)", "config": cfg,
-            "parallelism": "replicas" if world > 1 else "single GPU",
-            "roofline": dict(res["roofline"], peak_kind=peak_kind),
-            "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
-    line["roofline"]["frac_of"] = f"{peak_kind} HBM copy bandwidth"
-    if rank == 0 and not args.no_cpu_baseline:
-        v, cores, desc, tt = cpu_oracle_rate(mats, 0, 1, budget_s=12.0)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": desc + f" ({tt:.1f} s)"}
+    import gemm_rocmfp4_dequant_gb300 as rf4
+
+    if args.workload == "layer":
+        res = run_gemv(args, world, hbm, LAYER)
+        cfg["l2"] = (f"rotating {res['copies']} resident layer copies ({res['footprint_gb']} GB > 129 MB L2); "
+                     "inputs larger than L2")
+        line = base_line(args, world, res["value"], "GB/s", res["ms_per_step"], cfg, "f16")
+        line["roofline"] = gemv_roofline(res, hbm, peak_kind, LAYER, 0, 1)
+        line["e2e"] = res["e2e"]
+        line["gpu_launches"] = res["gpu_launches"]
+        line["clocks"] = res["clocks"]
+        line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
+        if not args.no_prefill:
+            pre, _ = run_prefill(PREFILL_M, bf16)
+            line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16", "peak": bf16, "peak_kind": f"{peak_kind} bf16 burst",
+                               "kernel": "gemm_tc_kernel", "bound": "tensor",
+                               "by_M": {str(m): v for m, v in pre.items()}}
+        if rank == 0 and not args.no_cpu_baseline:
+            v, cores, desc, tt = cpu_oracle_rate(LAYER, budget_s=12.0)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": desc + f" ({tt:.1f} s)"}
+    elif args.workload == "single":
+        res = run_single(args, world)
+        line = base_line(args, world, res["value"], "GB/s", res["ms_per_step"], cfg, "f16")
+        line.update(us_median=res["us_median"], gpu_launches=res["gpu_launches"], clocks=res["clocks"])
+    elif args.workload == "model":
+        res = run_model(args, world)
+        line = base_line(args, world, res["value"], "GB/s", res["ms_per_step"], cfg, "f16")
+        line.update(tok_s=round(res["tok_s"], 1), gpu_launches=res["gpu_launches"], clocks=res["clocks"],
+                    weight_gb=res["weight_gb"], frac_of_hbm_peak=round(res["value"] / hbm, 4))
+    elif args.workload == "sweep":
+        table = {}
+        for variant in (0, 1):
+            for M in (1, 2, 4, 8):
+                r = run_gemv(argparse.Namespace(steps=max(20, args.steps // 10), warmup=args.warmup), world, hbm,
+                             LAYER, variant=variant, M=M, with_e2e=False)
+                table[f"{'dual' if variant == 0 else 'fast'} M={M}"] = {
+                    "GB/s": round(r["value"], 1), "kernel_GB/s": round(r["achieved"], 1),
+                    "per_launch_us": r["per_launch_us"]}
+        first = table["dual M=1"]
+        line = base_line(args, world, first["GB/s"], "GB/s", 0.0, cfg, "f16")
+        line["sweep"] = table
+    else:  # prefill
+        pre, launches = run_prefill(PREFILL_M, bf16)
+        v = pre[4096]["tflops"]
+        line = base_line(args, world, v, "TFLOP/s", pre[4096]["layer_ms"], dict(cfg, headline="M=4096"), "bf16")
+        line["roofline"] = {"bound": "tensor", "achieved": v, "peak": bf16, "unit": "TFLOP/s",
+                            "frac": round(v / bf16, 4), "traffic": None, "kernel": "gemm_tc_kernel",
+                            "peak_kind": f"{peak_kind} bf16 burst"}
+        line["by_M"] = {str(m): r for m, r in pre.items()}
+        line["gpu_launches"] = launches
     if rank == 0:
         print(json.dumps(line))
 
