@@ -717,6 +717,8 @@ def main():
     ap.add_argument("--workload", default="layer", choices=["layer", "single", "sweep", "model", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill object out of the layer line")
+    ap.add_argument("--prefill-m", type=str, default=",".join(str(m) for m in PREFILL_M),
+                    help="comma-separated token counts of the prefill GEMM")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -762,7 +764,7 @@ def main():
         line["clocks"] = res["clocks"]
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
         if not args.no_prefill:
-            pre, _ = run_prefill(PREFILL_M, bf16)
+            pre, _ = run_prefill([int(m) for m in args.prefill_m.split(",")], bf16)
             line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16", "peak": bf16, "peak_kind": f"{peak_kind} bf16 burst",
                                "kernel": "gemm_tc_kernel", "bound": "tensor",
                                "by_M": {str(m): v for m, v in pre.items()}}
@@ -792,9 +794,11 @@ def main():
         line = base_line(args, world, first["GB/s"], "GB/s", 0.0, cfg, "f16")
         line["sweep"] = table
     else:  # prefill
-        pre, launches = run_prefill(PREFILL_M, bf16)
-        v = pre[4096]["tflops"]
-        line = base_line(args, world, v, "TFLOP/s", pre[4096]["layer_ms"], dict(cfg, headline="M=4096"), "bf16")
+        Ms = [int(m) for m in args.prefill_m.split(",")]
+        pre, launches = run_prefill(Ms, bf16)
+        head = 4096 if 4096 in pre else Ms[0]
+        v = pre[head]["tflops"]
+        line = base_line(args, world, v, "TFLOP/s", pre[head]["layer_ms"], dict(cfg, headline=f"M={head}"), "bf16")
         line["roofline"] = {"bound": "tensor", "achieved": v, "peak": bf16, "unit": "TFLOP/s",
                             "frac": round(v / bf16, 4), "traffic": None, "kernel": "gemm_tc_kernel",
                             "peak_kind": f"{peak_kind} bf16 burst"}

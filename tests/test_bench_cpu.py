@@ -1,0 +1,84 @@
+"""Host-side logic of bench.py, on the CPU: algorithmic byte counts, the traffic
+record's source check, clock-reason decoding, and the replica path (max over
+ranks, barriers) with two gloo ranks."""
+import hashlib
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def test_layer_and_model_bytes():
+    # packed bytes of the four layer matrices (dual, 18 B per 32 weights)
+    assert [bench.matrix_bytes(N, K) for _, N, K in bench.LAYER] == [20643840, 17694720, 100270080, 50135040]
+    # + 2 B per activation and 4 B per output at M = 1
+    assert bench.step_bytes(bench.LAYER) == sum(
+        N * K // 32 * 18 + 2 * K + 4 * N for _, N, K in bench.LAYER)
+    mats = [("x", N, K) for _ in range(bench.N_LAYERS) for (_, N, K) in bench.LAYER] + [bench.LM_HEAD]
+    assert bench.weight_bytes(mats) == 12517539840
+    assert bench.matrix_bytes(7168, 5120, variant=1) == 7168 * 160 * 17
+
+
+def test_traffic_record_needs_the_measured_source(tmp_path, monkeypatch):
+    src = tmp_path / "gemv.cu"
+    src.write_text("kernel v1\n")
+    rec = tmp_path / "rec.md"
+    sha = hashlib.sha256(b"kernel v1\n").hexdigest()
+    rec.write_text(f"notes\nsource_sha256: {sha}\ndram_bytes_per_launch: qkv=10, o=20, gate_up=30, down=40\n")
+    monkeypatch.setattr(bench, "GEMV_SOURCE", str(src))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
+    assert bench.gemv_traffic() == {"qkv": 10, "o": 20, "gate_up": 30, "down": 40}
+    src.write_text("kernel v2\n")  # kernel changed since the capture: no traffic figure
+    assert bench.gemv_traffic() is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.md"))
+    assert bench.gemv_traffic() is None
+
+
+def test_clock_summary_decodes_reasons():
+    c = bench.ClockSampler()
+    assert c.summary()["samples"] == 0
+    c.samples = [(2070.0, 0), (1980.0, 0x4), (2070.0, 0x40)]
+    c.max_mhz = 2070.0
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_peaks_read_the_measured_file():
+    hbm, bf16, bf16_s, kind = bench.peaks()
+    if os.path.exists(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured" and hbm > 1000 and bf16 > 100
+    else:
+        assert kind == "fallback"
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    w, r, _ = bench.dist_setup()
+    assert (w, r) == (world, rank)
+    bench.barrier(w)
+    out[rank] = bench.max_over_ranks(1.5 + rank, w)
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_replicas_take_the_max_over_ranks():
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    if torch.cuda.is_available():
+        pytest.skip("the gloo replica test runs on CPU-only hosts")
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True, start_method="spawn")
+    assert dict(out) == {0: 2.5, 1: 2.5}
