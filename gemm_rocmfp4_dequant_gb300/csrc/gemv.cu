@@ -44,6 +44,18 @@ namespace {
 
 constexpr int kWarps = kStreamWarpsPerCta;
 constexpr int kTileRows = 32;  // rows per unit / tile: two m16 MMA tiles sharing each B fragment
+constexpr int kRecFloats = kTileRows * 8;  // a global record: 32 rows x 8 columns
+
+// Shared-memory part of the reduction (MB <= 4): kWarps x 2 records of
+// 32 rows x MB columns, then one counter per warp.  A tile with parts in two
+// or more warps of a CTA continues from its first such warp w into w + 1, and
+// is w's last tile; so w identifies it.  With MB = 8 the records would cost
+// the kernel a CTA per SM, and every warp uses the global level directly.
+template <int MB>
+constexpr size_t cta_red_bytes() {
+  return MB <= 4 ? (size_t)kWarps * 2 * kTileRows * MB * 4 + kWarps * 4 : 0;
+}
+
 
 // Per-warp ring stage: 32 weight rows x SPAN bytes, then the matching slice of
 // MB activation rows (MB >= M, rounded to 1, 2, 4 or 8), KU fp16/bf16 values each.
@@ -60,7 +72,8 @@ constexpr int stages() {
 
 template <int V, int MB>
 constexpr size_t smem_bytes() {
-  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8 + 16;
+  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8 + 16 +
+         cta_red_bytes<MB>();
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -391,18 +404,142 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
   }
 }
 
+// Split-tile reduction.  A tile (32 rows x all K) whose spans are spread over
+// several warps is summed in two levels, each in a fixed order, so results
+// are bitwise reproducible:
+//   1. the warps of one CTA that hold parts of the tile add them in shared
+//      memory: each writes a record (32 rows x 8 columns) and bumps a
+//      per-tile shared counter; the last of them sums the records in warp
+//      (= K) order;
+//   2. if the tile also has parts in other CTAs, that warp writes the CTA's
+//      sum as a record in global memory and bumps a per-tile global counter;
+//      the last CTA sums the CTA records in CTA (= K) order and stores Y.
+// Nobody waits: whoever completes a count does the sum.
+
+struct CtaRed {
+  float* rec;     // [kWarps][2][32 * MB]
+  uint32_t* cnt;  // [kWarps], zero between tiles
+};
+
+// Record layout: row r, column m at rec[r * RS + m] (RS columns, M <= RS).
+// From the MMA fragments of acc (owner lanes only write).
+template <bool COL, int RS>
+RF4_DEV void write_record_frag(float* rec, const float (&acc)[2][4], int lane) {
+  const int q = lane >> 2, c = lane & 3;
+  const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
+  if ((COL && c != 0) || c0 >= RS) return;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = mt * 16 + q;
+    rec[r0 * RS + c0] = acc[mt][0];
+    rec[(r0 + 8) * RS + c0] = acc[mt][2];
+    if (!COL) {
+      rec[r0 * RS + c1] = acc[mt][1];
+      rec[(r0 + 8) * RS + c1] = acc[mt][3];
+    }
+  }
+}
+
+// Record layout from row-per-lane sums (lane r holds row r).
+template <int RS>
+RF4_DEV void write_record_rows(float* rec, const float (&sum)[8], int lane, int M) {
+  if (M == 1) {
+    rec[lane * RS] = sum[0];
+  } else if constexpr (RS % 4 == 0) {
+#pragma unroll
+    for (int h = 0; h < RS / 4; ++h)
+      reinterpret_cast<float4*>(rec + lane * RS)[h] =
+          make_float4(sum[4 * h], sum[4 * h + 1], sum[4 * h + 2], sum[4 * h + 3]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < RS; ++m) rec[lane * RS + m] = sum[m];
+  }
+}
+
+// Row-per-lane sum of records first .. last (in that order) at
+// base + (2 * (idx - idx0) + slot) * 32 * RS; record `first` is in slot
+// `slot_first`, the others in slot 0.  Global records are read through L2.
+template <bool GLOBAL, int RS>
+RF4_DEV void sum_records(const float* base, int64_t idx0, int64_t first, int64_t last, int slot_first, int lane, int M,
+                         float (&sum)[8]) {
+  constexpr int RF = kTileRows * RS;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) sum[m] = 0.f;
+  if (M == 1) {
+    for (int64_t w0 = first; w0 <= last; w0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t w = w0 + k;
+        const float* r = base + (2 * (w - idx0) + (w == first ? slot_first : 0)) * RF + lane * RS;
+        v[k] = w <= last ? (GLOBAL ? __ldcg(r) : *r) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w0 + k <= last) sum[0] += v[k];
+    }
+  } else {
+    // RS = 2, 4 or 8 columns per row: 8-, 16- or 32-byte aligned, read as vectors
+    for (int64_t w0 = first; w0 <= last; w0 += 4) {
+      float v[4][RS];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t w = w0 + k;
+        const float* r = base + (2 * (w - idx0) + (w == first ? slot_first : 0)) * RF + lane * RS;
+        if (w <= last) {
+          if constexpr (RS == 2) {
+            const float2 a = GLOBAL ? __ldcg(reinterpret_cast<const float2*>(r)) : *reinterpret_cast<const float2*>(r);
+            v[k][0] = a.x;
+            v[k][1] = a.y;
+          } else {
+#pragma unroll
+            for (int h = 0; h < RS / 4; ++h) {
+              const float4* r4 = reinterpret_cast<const float4*>(r) + h;
+              const float4 a = GLOBAL ? __ldcg(r4) : *r4;
+              v[k][4 * h] = a.x;
+              v[k][4 * h + 1] = a.y;
+              v[k][4 * h + 2] = a.z;
+              v[k][4 * h + 3] = a.w;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < RS; ++m) v[k][m] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (w0 + k <= last)
+#pragma unroll
+          for (int m = 0; m < RS; ++m) sum[m] += v[k][m];
+    }
+  }
+}
+
+RF4_DEV void store_rows(float* __restrict__ Y, int64_t N, int64_t row, const float (&sum)[8], int M) {
+  if (row < N)
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if (m < M) Y[m * N + row] = sum[m];
+}
+
+RF4_DEV uint32_t shared_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
 // End of tile t of product op for this warp (its spans [js, j] are in acc):
 // store the tile if the warp covered all of it, else hand its partial to the
 // split-tile reduction.  Resets acc.
 template <int MB, int NOPS>
-RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_t wg, int t, int t_first, int js,
-                         int j, int lane, float (&acc)[2][4]) {
+RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_t wg, int t, int js, int j, int lane,
+                         float (&acc)[2][4], const CtaRed& red) {
   constexpr bool COL = MB == 1;
+  constexpr bool LOCAL = cta_red_bytes<MB>() > 0;  // level 1 in shared memory
   const int M = p.M;
   const int64_t N = op.N, S = op.nspans, U = op.units, wact = op.wact;
   float* __restrict__ Y = op.Y;
-  float* __restrict__ ws = p.ws;
-  uint32_t* __restrict__ cnt = p.cnt;
   const int q = lane >> 2, c = lane & 3;
   // Bring the partial sums to lanes: in column-split mode add the two halves
   // and the four lanes of each quad (fixed order), so lane (q, 0) holds rows
@@ -420,96 +557,73 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
       acc[mt][1] = acc[mt][3] = 0.f;
     }
   }
-  const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
-  const bool owner = !COL || c == 0;  // lanes holding finished values
-  bool store = true;
-  if (!(js == 0 && j == S - 1)) {
-    float* rec = ws + (2 * wg + (t == t_first ? 0 : 1)) * (kTileRows * 8);
-    if (owner) {
+  const int64_t row = (int64_t)t * kTileRows + lane;
+  if (js == 0 && j == S - 1) {
+    // the whole tile is this warp's
+    const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
+    if (!COL || c == 0) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        const int r0 = mt * 16 + q;
-        rec[r0 * 8 + c0] = acc[mt][0];
-        rec[(r0 + 8) * 8 + c0] = acc[mt][2];
-        if (!COL) {
-          rec[r0 * 8 + c1] = acc[mt][1];
-          rec[(r0 + 8) * 8 + c1] = acc[mt][3];
+        const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
+        if (c0 < M) {
+          if (ra < N) Y[c0 * N + ra] = acc[mt][0];
+          if (rb < N) Y[c0 * N + rb] = acc[mt][2];
+        }
+        if (!COL && c1 < M) {
+          if (ra < N) Y[c1 * N + ra] = acc[mt][1];
+          if (rb < N) Y[c1 * N + rb] = acc[mt][3];
         }
       }
     }
-    __syncwarp();  // orders the warp's partial stores before lane 0's release
+  } else {
     const int64_t tS = (int64_t)t * S;
-    const int64_t wf = owner_of(tS, U, wact), wl = owner_of(tS + S - 1, U, wact);
-    uint32_t old = 0;
-    if (lane == 0) old = atomic_add_acq_rel_gpu(&cnt[wf], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
-    if ((int64_t)old == wl - wf) {
-      // Last contributor: lane r sums row r of the tile over all records in
-      // contributor (= K) order and stores it.  Every contributor after the
-      // first starts inside tile t (record slot 0); the first is in slot 1 if
-      // it started before the tile.
-      const bool first_in_slot1 = U * wf / wact < tS;
-      const int64_t row = (int64_t)t * kTileRows + lane;
-      if (M == 1) {
-        float sum = 0.f;
-        for (int64_t w0 = wf; w0 <= wl; w0 += 8) {
-          float v[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int64_t w2 = w0 + k;
-            const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-            v[k] = w2 <= wl ? __ldcg(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8) : 0.f;
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (w0 + k <= wl) sum += v[k];
-        }
-        if (row < N) Y[row] = sum;
-      } else {
-        // the 8 column slots of row `lane` are 32 contiguous bytes per record
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
-          float4 v[4][2];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int64_t w2 = w0 + k;
-            const int slot = (w2 == wf && first_in_slot1) ? 1 : 0;
-            const float4* r2 = reinterpret_cast<const float4*>(ws + (2 * w2 + slot) * (kTileRows * 8) + lane * 8);
-            if (w2 <= wl) {
-              v[k][0] = __ldcg(r2);
-              v[k][1] = __ldcg(r2 + 1);
-            } else {
-              v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (w0 + k <= wl) {
-              sum[0] += v[k][0].x; sum[1] += v[k][0].y; sum[2] += v[k][0].z; sum[3] += v[k][0].w;
-              sum[4] += v[k][1].x; sum[5] += v[k][1].y; sum[6] += v[k][1].z; sum[7] += v[k][1].w;
-            }
-        }
-        if (row < N)
-#pragma unroll
-          for (int m = 0; m < 8; ++m)
-            if (m < M) Y[m * N + row] = sum[m];
-      }
+    const int64_t wf = owner_of(tS, U, wact), wl = owner_of(tS + S - 1, U, wact);  // the tile's warps
+    const int64_t cta = wg / kWarps, w0c = cta * kWarps;
+    const int64_t wlast_cta = (w0c + kWarps < wact ? w0c + kWarps : wact) - 1;
+    const int64_t lf = wf > w0c ? wf : w0c, ll = wl < wlast_cta ? wl : wlast_cta;  // the tile's warps in this CTA
+    const int slot_wf = U * wf / wact < tS ? 1 : 0;  // the first warp started before the tile
+    const int key = (int)(lf - w0c);
+    float sum[8];
+    bool pass = true;     // this warp carries the CTA's part on
+    bool rows = false;    // ... as row-per-lane sums (else as fragments in acc)
+    if (LOCAL && ll > lf) {
+      // level 1: the CTA's warps meet in shared memory
+      write_record_frag<COL, MB>(red.rec + ((wg - w0c) * 2 + (wg == wf ? slot_wf : 0)) * (kTileRows * MB), acc, lane);
       __syncwarp();
-      if (lane == 0) store_relaxed_gpu(&cnt[wf], 0u);
-    }
-    store = false;  // the last contributor stored above
-  }
-  if (store && owner) {
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
-      if (c0 < M) {
-        if (ra < N) Y[c0 * N + ra] = acc[mt][0];
-        if (rb < N) Y[c0 * N + rb] = acc[mt][2];
+      uint32_t old = 0;
+      if (lane == 0) old = shared_add_acq_rel(&red.cnt[key], 1u);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      pass = (int64_t)old == ll - lf;
+      if (pass) {
+        sum_records<false, MB>(red.rec, w0c, lf, ll, lf == wf ? slot_wf : 0, lane, M, sum);
+        rows = true;
+        __syncwarp();
+        if (lane == 0) red.cnt[key] = 0u;
       }
-      if (!COL && c1 < M) {
-        if (ra < N) Y[c1 * N + ra] = acc[mt][1];
-        if (rb < N) Y[c1 * N + rb] = acc[mt][3];
+    }
+    if (pass) {
+      // level 2 counts CTAs (or warps, without level 1)
+      const int64_t per = LOCAL ? kWarps : 1;
+      const int64_t me = wg / per, uf = wf / per, ul = wl / per;
+      if (uf == ul) {
+        // every part was in this CTA
+        store_rows(Y, N, row, sum, M);
+      } else {
+        // one record per contributor in global memory, counted per tile
+        const int slot_uf = U * (uf * per) / wact < tS ? 1 : 0;
+        float* grec = p.ws + (2 * me + (me == uf ? slot_uf : 0)) * kRecFloats;
+        if (rows) write_record_rows<8>(grec, sum, lane, M);
+        else write_record_frag<COL, 8>(grec, acc, lane);
+        __syncwarp();  // orders the warp's record stores before lane 0's release
+        uint32_t old = 0;
+        if (lane == 0) old = atomic_add_acq_rel_gpu(&p.cnt[uf], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
+        if ((int64_t)old == ul - uf) {
+          sum_records<true, 8>(p.ws, 0, uf, ul, slot_uf, lane, M, sum);
+          store_rows(Y, N, row, sum, M);
+          __syncwarp();
+          if (lane == 0) store_relaxed_gpu(&p.cnt[uf], 0u);
+        }
       }
     }
   }
@@ -542,17 +656,22 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
 
   uint8_t* ring = smem + (size_t)warp * NS * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * SB) + warp * NS;
-  // chain barrier words of the CTA (after every warp's stage barriers)
+  // chain barrier words of the CTA (after every warp's stage barriers), then
+  // the shared part of the split-tile reduction
   uint32_t* cta_count = reinterpret_cast<uint32_t*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
   uint32_t* cta_gen = cta_count + 1;
+  CtaRed red;
+  red.rec = reinterpret_cast<float*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + 16);
+  red.cnt = reinterpret_cast<uint32_t*>(red.rec + kWarps * 2 * kTileRows * MB);  // used only if cta_red_bytes<MB>() > 0
   const int64_t cta_first = (int64_t)blockIdx.x * kWarps;
   const uint32_t warps_here = (uint32_t)(wact - cta_first < kWarps ? wact - cta_first : kWarps);
   const uint32_t ctas = (uint32_t)((wact + kWarps - 1) / kWarps);
-  if (NOPS > 1 && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     *cta_count = 0u;
     *cta_gen = 0u;
   }
-  if (NOPS > 1) __syncthreads();  // every thread of the CTA gets here: inactive warps return below
+  if (cta_red_bytes<MB>() > 0 && threadIdx.x < kWarps) red.cnt[threadIdx.x] = 0u;
+  __syncthreads();  // every thread of the CTA gets here: inactive warps return below
   if (wg >= wact) return;
   if (lane == 0) {
     for (int g = 0; g < p.nops && g < 4; ++g)
@@ -630,7 +749,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
       __syncwarp();
       fence_proxy_async();
       if (j == Si - 1 || k == nunits - 1) {
-        finish_tile<MB>(p, op, wg, t, t_first, js, j, lane, acc);
+        finish_tile<MB>(p, op, wg, t, js, j, lane, acc, red);
         js = 0;
       }
       if (++j == Si) {
