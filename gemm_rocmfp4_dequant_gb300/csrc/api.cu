@@ -22,6 +22,8 @@ struct DeviceState {
   uint32_t* cnt = nullptr;           // wmax split counters
   uint32_t* err = nullptr;           // kernel error bits
   uint32_t* gbar = nullptr;          // grid barrier counter of chained launches
+  float* tcws = nullptr;             // tensor-core kernel: split-tile partials
+  uint32_t* tccnt = nullptr;         // tensor-core kernel: split-tile counters
   unsigned long long* vfirst = nullptr;
 };
 
@@ -79,6 +81,11 @@ rocmfp4_status device_state(DeviceState** out) {
     if ((e = cudaMemset(d.gbar, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaMalloc(&d.vfirst, sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(d.cnt, 0, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    if ((e = cudaMalloc(&d.tcws, sizeof(float) * tc_ws_floats(d.sms))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&d.tccnt, sizeof(uint32_t) * tc_cnt_words(d.sms))) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(d.tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d.sms))) != cudaSuccess)
+      return cuda_fail(e, "cudaMemset");
     if ((e = cudaMemset(d.err, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     d.ready = true;
@@ -122,7 +129,7 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
   const bool tc_ok = M > 8 && K % tc_k_multiple(variant) == 0 && aligned16(W) && aligned16(X) &&
                      M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31);
   if (tc_ok) {
-    TcArgs a{static_cast<const uint8_t*>(W), Xh, Y, M, N, K, row_bytes, d->err};
+    TcArgs a{static_cast<const uint8_t*>(W), Xh, Y, M, N, K, row_bytes, d->tcws, d->tccnt, d->err};
     cudaError_t e = launch_gemm_tc(variant, act, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
     g_launches.fetch_add(1);
@@ -345,6 +352,7 @@ uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream) {
     cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
     cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
     cudaMemsetAsync(d->gbar, 0, sizeof(uint32_t), s);
+    cudaMemsetAsync(d->tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d->sms), s);
     cudaStreamSynchronize(s);
   }
   return bits;
@@ -377,6 +385,9 @@ void rocmfp4_shutdown(void) {
     cudaFree(d.ws);
     cudaFree(d.cnt);
     cudaFree(d.err);
+    cudaFree(d.gbar);
+    cudaFree(d.tcws);
+    cudaFree(d.tccnt);
     cudaFree(d.vfirst);
     d = DeviceState{};
   }

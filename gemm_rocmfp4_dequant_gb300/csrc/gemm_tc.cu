@@ -45,6 +45,7 @@
 // precedes the tensor-memory release.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "common.cuh"
@@ -126,6 +127,123 @@ struct Raster {
     n0 = (in_g / gsize) * kTcRows;
   }
 };
+
+// Work items.  Tiles 0 .. dp_tiles-1 are dealt out whole, round robin (full
+// waves of the grid).  The remaining tiles form the split region: its
+// tiles x nch raw chunks are numbered tile-major and cut into gridDim.x
+// contiguous ranges of near-equal length, one per CTA, so every SM gets the
+// same amount of work however the tile count falls against the SM count.
+// A range yields one item per tile it touches: (tile, chunk range).
+struct Sched {
+  int dp_tiles;  // tiles dealt out whole
+  int nch;       // raw chunks per tile (K / KR)
+  int64_t usk;   // chunks of the split region
+  RF4_DEV int64_t start(int b) const { return (int64_t)b * usk / gridDim.x; }
+  // The CTA whose range holds chunk u: the largest b with start(b) <= u.
+  RF4_DEV int owner(int64_t u) const { return (int)(((u + 1) * (int64_t)gridDim.x - 1) / usk); }
+};
+
+struct Item {
+  int t, cb, ce;  // tile and its raw chunks [cb, ce)
+};
+
+struct ItemIter {
+  int next_dp;
+  int64_t u, uend;
+  RF4_DEV explicit ItemIter(const Sched& s)
+      : next_dp((int)blockIdx.x), u(s.start((int)blockIdx.x)), uend(s.start((int)blockIdx.x + 1)) {}
+  RF4_DEV bool next(const Sched& s, Item& it) {
+    if (next_dp < s.dp_tiles) {
+      it.t = next_dp;
+      it.cb = 0;
+      it.ce = s.nch;
+      next_dp += (int)gridDim.x;
+      return true;
+    }
+    if (u >= uend) return false;
+    const int64_t tr = u / s.nch;
+    it.t = s.dp_tiles + (int)tr;
+    it.cb = (int)(u - tr * s.nch);
+    const int64_t left = uend - u;
+    it.ce = left < (int64_t)(s.nch - it.cb) ? it.cb + (int)left : s.nch;
+    u += it.ce - it.cb;
+    return true;
+  }
+};
+
+constexpr int kSubsPerChain = kChainK / kSubK;
+constexpr size_t kSlotFloats = (size_t)kTcRows * kMaxNT;  // one partial tile in the split workspace
+
+RF4_DEV void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kOutThreads) : "memory"); }
+
+// One partial tile in the split workspace: [token group g][quad q][row][4],
+// token 16 g + 4 q + i of weight row `row` at element i, so that a warp's
+// float4 access of one (g, q) covers 512 contiguous bytes.
+RF4_DEV size_t part_index(int g, int q, int row) { return (((size_t)g * 4 + q) * kTcRows + row) * 4; }
+
+// The parts of one split tile: part k is CTA (bfirst + k)'s, in its slot
+// 2 (bfirst + k), except that part 0 sits in slot 2 bfirst + 1 when it ends
+// that CTA's range instead of starting it.
+struct Parts {
+  const float* ws;
+  int bfirst, nparts;
+  bool first_tail;
+  RF4_DEV const float* slot(int k) const {
+    return ws + (size_t)(2 * (bfirst + k) + (k == 0 && first_tail ? 1 : 0)) * kSlotFloats;
+  }
+  // s = part 0 + part 1 + ... (in this order) for 16 tokens of one weight row;
+  // the loads of kBatch parts are in flight together.
+  static constexpr int kBatch = 2;
+  RF4_DEV void sum(int g, int row, float4 (&s)[4]) const {
+#pragma unroll 1
+    for (int k0 = 0; k0 < nparts; k0 += kBatch) {
+      float4 v[kBatch][4];
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk)
+        if (k0 + kk < nparts) {
+          const float* base = slot(k0 + kk);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[kk][q] = __ldcg(reinterpret_cast<const float4*>(base + part_index(g, q, row)));
+        }
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk)
+        if (k0 + kk < nparts) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (k0 + kk == 0) {
+              s[q] = v[kk][q];
+            } else {
+              s[q].x += v[kk][q].x;
+              s[q].y += v[kk][q].y;
+              s[q].z += v[kk][q].z;
+              s[q].w += v[kk][q].w;
+            }
+          }
+        }
+    }
+  }
+};
+
+// Y[m + j][n] = tokens j = 0..15 of a summed split tile (s4[q] holds tokens
+// 4q .. 4q+3); a warp's lanes hold consecutive n, so each store is coalesced.
+RF4_DEV void store_fix16(const float4 (&s4)[4], float* Y, int M, int N, int m, int n) {
+  if (n >= N) return;
+  const float v[16] = {s4[0].x, s4[0].y, s4[0].z, s4[0].w, s4[1].x, s4[1].y, s4[1].z, s4[1].w,
+                       s4[2].x, s4[2].y, s4[2].z, s4[2].w, s4[3].x, s4[3].y, s4[3].z, s4[3].w};
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (m + j < M) Y[(size_t)(m + j) * N + n] = v[j];
+}
+
+RF4_DEV Parts tile_parts(const Sched& sc, const float* ws, int t) {
+  const int64_t t0 = (int64_t)(t - sc.dp_tiles) * sc.nch;
+  Parts p;
+  p.ws = ws;
+  p.bfirst = sc.owner(t0);
+  p.nparts = sc.owner(t0 + sc.nch - 1) - p.bfirst + 1;
+  p.first_tail = sc.start(p.bfirst) != t0;
+  return p;
+}
 
 RF4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 RF4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -239,6 +357,57 @@ RF4_DEV void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
       : "memory");
 }
 
+// AND of v over the 128 output threads (named barrier 1).
+RF4_DEV bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kOutThreads)
+      : "memory");
+  return r != 0;
+}
+
+// Stores of one output warp: 16 tokens x its 32 outputs (tensor-memory lanes)
+// of Y, through shared memory and a TMA tensor store when Y's rows are
+// 16-byte aligned (rows past M and columns past N are not written), else
+// plain stores.
+template <int EBUF>
+struct Emit {
+  uint8_t* ebuf;  // EBUF buffers of kEpiBytes
+  int ebi;
+  int quarter, lane, tma_y;
+  const CUtensorMap* tmy;
+  float* Y;
+  int M, N;
+  RF4_DEV void store(const uint32_t (&a)[16], int m, int n0) {
+    if (tma_y) {
+      uint8_t* buf = ebuf + (uint32_t)ebi * kEpiBytes;
+      if (lane == 0) bulk_wait_group_read<EBUF - 1>();  // the buffer's previous store has read it
+      __syncwarp();
+      float* fb = reinterpret_cast<float*>(buf);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) fb[j * 32 + lane] = __uint_as_float(a[j]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (n0 + quarter * 32 < N && m < M) tma_store_2d(tmy, n0 + quarter * 32, m, smem_addr(buf));
+        bulk_commit_group();
+      }
+      ebi = ebi + 1 == EBUF ? 0 : ebi + 1;
+    } else {
+      const int n = n0 + quarter * 32 + lane;
+      if (n < N) {
+        float* y = Y + (size_t)m * N + n;
+        const int mlim = M - m;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < mlim) y[(size_t)j * N] = __uint_as_float(a[j]);
+      }
+    }
+  }
+};
+
 // Ring position: stage index and the parity of its current use.
 struct Ring {
   uint32_t stage = 0;
@@ -259,6 +428,7 @@ struct Bars {
   uint64_t* cfull;    // chain finished (MMA commit)
   uint64_t* cfree;    // slot C folded into R (output warps)
   uint64_t* accfree;  // epilogue has read R and C (output warps)
+  uint64_t* fixbar;   // split fix-up: bulk copies of the parts (TMA bytes)
 };
 
 // Slice S (two blocks, 64 K) of the raw chunk, for this thread's weight row,
@@ -320,7 +490,8 @@ template <int V, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                    const __grid_constant__ CUtensorMap tmy, int tma_y, float* __restrict__ Y, int M, int N, int K,
-                   int nt, int mtiles, int ntiles, int group_m, uint32_t* __restrict__ err) {
+                   int nt, int mtiles, int ntiles, int group_m, Sched sched, float* __restrict__ ws,
+                   uint32_t* __restrict__ tcnt, uint32_t* __restrict__ err) {
   using F = TcFmt<V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -337,13 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.cfull = b.rempty + F::RSTAGES;
   b.cfree = b.cfull + 1;
   b.accfree = b.cfree + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.accfree + 1);
+  b.fixbar = b.accfree + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 1);
+  // Split tiles whose last part this CTA finished (at most two: a CTA's
+  // split range has a part at each end), summed by all threads after the
+  // roles end: {count, then (tile, m0, n0) per tile}.
+  volatile int* fix = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Raster raster{mtiles, ntiles, group_m, nt};
-  const int ntotal = mtiles * ntiles;
-  const int nsub = K / kSubK, nchunks = K / F::KR;
-  const int nchains = (K + kChainK - 1) / kChainK;
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < S; ++i) {
@@ -357,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(b.cfull), 1);
     mbar_init(smem_addr(b.cfree), kOutThreads);
     mbar_init(smem_addr(b.accfree), kOutThreads);
+    mbar_init(smem_addr(b.fixbar), 1);
+    fix[0] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -375,10 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
       Ring r;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
+      ItemIter it(sched);
+      Item w;
+      while (ok && it.next(sched, w)) {
         int m0, n0;
-        raster.tile(t, m0, n0);
-        for (int ks = 0; ks < nsub; ++ks, r.next(S)) {
+        raster.tile(w.t, m0, n0);
+        for (int ks = w.cb * F::SUBS; ks < w.ce * F::SUBS; ++ks, r.next(S)) {
           if (!mbar_wait_bounded(smem_addr(&b.empty[r.stage]), r.phase ^ 1u)) {
             ok = false;
             break;
@@ -396,10 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
       Ring r;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
+      ItemIter it(sched);
+      Item w;
+      while (ok && it.next(sched, w)) {
         int m0, n0;
-        raster.tile(t, m0, n0);
-        for (int rc = 0; rc < nchunks; ++rc, r.next(F::RSTAGES)) {
+        raster.tile(w.t, m0, n0);
+        for (int rc = w.cb; rc < w.ce; ++rc, r.next(F::RSTAGES)) {
           if (!mbar_wait_bounded(smem_addr(&b.rempty[r.stage]), r.phase ^ 1u)) {
             ok = false;
             break;
@@ -421,15 +600,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       Ring r;
       uint32_t n_cfree = 0, n_accfree = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
-        // both slots must have been read by the previous tile's epilogue
-        if (t != (int)blockIdx.x && !mbar_wait_bounded(smem_addr(b.accfree), (n_accfree++) & 1u)) {
+      ItemIter it(sched);
+      Item w;
+      for (bool first = true; ok && it.next(sched, w); first = false) {
+        // both slots must have been read by the previous item's epilogue
+        if (!first && !mbar_wait_bounded(smem_addr(b.accfree), (n_accfree++) & 1u)) {
           ok = false;
           break;
         }
-        int ks = 0;
+        const int s0 = w.cb * F::SUBS, nsub = (w.ce - w.cb) * F::SUBS;
+        const int nchains = (nsub + kSubsPerChain - 1) / kSubsPerChain;
+        int ks = s0;
         for (int c = 0; c < nchains && ok; ++c) {
-          const int kend = (int)((int64_t)(c + 1) * nsub / nchains);
+          const int kend = s0 + (int)((int64_t)(c + 1) * nsub / nchains);
           // chains 2.. reuse slot C once the output warps have folded it into R
           if (c >= 2 && !mbar_wait_bounded(smem_addr(b.cfree), (n_cfree++) & 1u)) {
             ok = false;
@@ -464,8 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ring rr, ring;
     if (half) ring.next(S);
     bool ok = true;
-    for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
-      for (int rc = 0; rc < nchunks; ++rc, rr.next(F::RSTAGES)) {
+    ItemIter it(sched);
+    Item w;
+    while (ok && it.next(sched, w)) {
+      for (int rc = w.cb; rc < w.ce; ++rc, rr.next(F::RSTAGES)) {
         if (!warp_wait(smem_addr(&b.rfull[rr.stage]), rr.phase)) {
           ok = false;
           break;
@@ -481,20 +666,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 12) {
     // ---- chain folds and epilogue ----
     const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // tensor-memory lane = weight row of the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t slot_r = tmem + lane_off, slot_c = tmem + lane_off + plan.cstride;
-    uint8_t* ebuf = smem + plan.off_epi + (uint32_t)quarter * F::EBUF * kEpiBytes;
-    int ebi = 0;
+    Emit<F::EBUF> out{smem + plan.off_epi + (uint32_t)quarter * F::EBUF * kEpiBytes, 0, quarter, lane, tma_y, &tmy, Y,
+                      M, N};
     uint32_t n_cfull = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntotal && ok; t += gridDim.x) {
+    ItemIter it(sched);
+    Item w;
+    while (ok && it.next(sched, w)) {
       int m0, n0;
-      raster.tile(t, m0, n0);
+      raster.tile(w.t, m0, n0);
+      const int nsub = (w.ce - w.cb) * F::SUBS;
+      const int nchains = (nsub + kSubsPerChain - 1) / kSubsPerChain;
+      const bool whole = w.cb == 0 && w.ce == sched.nch;
+      const int64_t t0 = (int64_t)(w.t - sched.dp_tiles) * sched.nch;  // first chunk of a split tile
+      // A part of a split tile goes to the CTA's workspace slot 2b (the part
+      // that starts its range) or 2b + 1 (the part that ends it).
+      float* part = whole ? nullptr
+                          : ws + (size_t)(2 * blockIdx.x + (t0 + w.cb == sched.start((int)blockIdx.x) ? 0 : 1)) *
+                                     kSlotFloats;
       for (int c = nchains > 1 ? 1 : 0; c < nchains; ++c) {  // chain 0 of several stays in R
-        if (!warp_wait(smem_addr(b.cfull), (n_cfull++) & 1u)) {
-          ok = false;
-          break;
-        }
+        // the four output warps leave together, so their named barriers stay matched
+        if (!(ok = epi_all(warp_wait(smem_addr(b.cfull), (n_cfull++) & 1u)))) break;
         tc_fence_after();
         if (c + 1 < nchains) {
           // R += C, then C may take the next chain
@@ -513,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_addr(b.cfree));
           continue;
         }
-        // last chain: Y = R (+ C), 16 tokens at a time
+        // last chain: R (+ C), 16 tokens at a time, to Y or to the workspace
 #pragma unroll 1
         for (int c0 = 0; c0 < nt; c0 += 16) {
           uint32_t a[16], v[16];
@@ -526,34 +721,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (c0 + 16 >= nt) {
             tc_fence_before();
-            mbar_arrive(smem_addr(b.accfree));  // both slots read: the next tile may start
+            mbar_arrive(smem_addr(b.accfree));  // both slots read: the next item may start
           }
-          if (tma_y) {
-            // through shared memory: a [16 tokens][32 outputs] box, stored by TMA
-            // (rows past M and columns past N are not written)
-            uint8_t* buf = ebuf + (uint32_t)ebi * kEpiBytes;
-            if (lane == 0) bulk_wait_group_read<F::EBUF - 1>();  // the buffer's previous store has read it
-            __syncwarp();
-            float* fb = reinterpret_cast<float*>(buf);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) fb[j * 32 + lane] = __uint_as_float(a[j]);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
-              if (n0 + quarter * 32 < N && m0 + c0 < M) tma_store_2d(&tmy, n0 + quarter * 32, m0 + c0, smem_addr(buf));
-              bulk_commit_group();
-            }
-            ebi = ebi + 1 == F::EBUF ? 0 : ebi + 1;
+          if (whole) {
+            out.store(a, m0 + c0, n0);
           } else {
-            const int n = n0 + quarter * 32 + lane;
-            if (n < N) {
-              float* y = Y + (size_t)(m0 + c0) * N + n;
-              const int mlim = M - (m0 + c0);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < mlim) y[(size_t)j * N] = __uint_as_float(a[j]);
-            }
+            for (int q = 0; q < 4; ++q)
+              __stcg(reinterpret_cast<float4*>(part + part_index(c0 / 16, q, row)),
+                     make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
+                                 __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3])));
           }
+        }
+      }
+      if (!ok || whole) continue;
+      // Split tile: count the finished parts.  The CTA that finishes the last
+      // one adds all parts in chunk order (a fixed order, whichever CTA it
+      // is) once its roles have ended.  Nothing waits on another CTA.
+      const int nparts = tile_parts(sched, ws, w.t).nparts;
+      epi_bar_sync();  // every output thread's part stores precede the count
+      if (row == 0) {
+        __threadfence();  // this CTA's part is visible before the count
+        const uint32_t done = atomicAdd(&tcnt[w.t - sched.dp_tiles], 1u) + 1u;
+        if (done == (uint32_t)nparts) {
+          __threadfence();                              // the other parts are visible after the count
+          atomicExch(&tcnt[w.t - sched.dp_tiles], 0u);  // ready for the next launch
+          const int i = fix[0];
+          fix[1 + 3 * i] = w.t;
+          fix[2 + 3 * i] = m0;
+          fix[3 + 3 * i] = n0;
+          fix[0] = i + 1;
         }
       }
     }
@@ -567,6 +764,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(plan.tmem_cols));
   }
+  // ---- split fix-up: all threads, shared memory free of the main loop ----
+  const int nfix = fix[0];
+  uint32_t fix_phase = 0;
+  bool fix_ok = true;
+#pragma unroll 1
+  for (int f = 0; f < nfix; ++f) {
+    const Parts parts = tile_parts(sched, ws, fix[1 + 3 * f]);
+    const int m0 = fix[2 + 3 * f], n0 = fix[3 + 3 * f];
+    const int groups = nt / 16;
+    constexpr uint32_t kGroupBytes = kTcRows * 16 * 4;  // one part, 16 tokens
+    // token groups per window: every part's window fits in the stage and raw rings
+    const int win = min(groups, (int)(plan.off_epi / ((uint32_t)parts.nparts * kGroupBytes)));
+    if (win == 0) {
+      // too many parts for shared memory: sum straight from the workspace
+#pragma unroll 1
+      for (int pi = threadIdx.x; pi < kTcRows * groups; pi += kThreads) {
+        const int row = pi % kTcRows, g = pi / kTcRows;
+        float4 s4[4];
+        parts.sum(g, row, s4);
+        store_fix16(s4, Y, M, N, m0 + 16 * g, n0 + row);
+      }
+      continue;
+    }
+#pragma unroll 1
+    for (int g0 = 0; g0 < groups; g0 += win) {
+      const int gw = min(win, groups - g0);
+      const uint32_t pbytes = (uint32_t)gw * kGroupBytes;
+      if (threadIdx.x == 0) {
+        // the rings' last generic-proxy accesses, and the parts acquired
+        // through the counter, come before the bulk copies
+        asm volatile("fence.proxy.async;" ::: "memory");
+        mbar_arrive_expect_tx(smem_addr(b.fixbar), pbytes * (uint32_t)parts.nparts);
+        for (int k = 0; k < parts.nparts; ++k)
+          bulk_g2s(smem_addr(smem + (size_t)k * pbytes), parts.slot(k) + (size_t)g0 * kTcRows * 16, pbytes,
+                   smem_addr(b.fixbar));
+      }
+      fix_ok = mbar_wait_bounded(smem_addr(b.fixbar), fix_phase) && fix_ok;
+      fix_phase ^= 1u;
+#pragma unroll 1
+      for (int pi = threadIdx.x; pi < kTcRows * gw; pi += kThreads) {
+        const int row = pi % kTcRows, gl = pi / kTcRows;
+        float4 s4[4];
+#pragma unroll 1
+        for (int k = 0; k < parts.nparts; ++k) {
+          const float4* src = reinterpret_cast<const float4*>(smem + (size_t)k * pbytes) + (size_t)gl * 4 * kTcRows + row;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = src[q * kTcRows];
+            if (k == 0) {
+              s4[q] = v;
+            } else {
+              s4[q].x += v.x;
+              s4[q].y += v.y;
+              s4[q].z += v.z;
+              s4[q].w += v.w;
+            }
+          }
+        }
+        store_fix16(s4, Y, M, N, m0 + 16 * (g0 + gl), n0 + row);
+      }
+      __syncthreads();  // the window is consumed before the next copies overwrite it
+    }
+  }
+  if (!fix_ok) atomicOr(err, kErrWaitTimeout);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -588,6 +849,8 @@ int g_sms = 0;
 }  // namespace
 
 int tc_k_multiple(int variant) { return variant == 0 ? TcFmt<0>::KR : TcFmt<1>::KR; }
+size_t tc_ws_floats(int sms) { return 2 * (size_t)sms * kSlotFloats; }
+size_t tc_cnt_words(int sms) { return 2 * (size_t)sms; }
 
 cudaError_t tc_prepare() {
   if (!g_encode) {
@@ -655,11 +918,34 @@ cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s
   }
   const TcPlan plan = tc_plan(variant, nt);
   const int64_t tiles = mtiles * ntiles;
-  const int grid = (int)(tiles < g_sms ? tiles : g_sms);
+  const int64_t nch = a.K / tc_k_multiple(variant);
+  // Whole tiles in full waves of the grid; when the tile count is not a
+  // multiple of the SM count, the last wave and a half (or, below one wave,
+  // every tile) are split by K so that each SM gets the same number of raw
+  // chunks, but no fewer than about 1024 K each.
+  const int64_t min_chunks = 1024 / tc_k_multiple(variant);
+  Sched sched{(int)tiles, (int)nch, 0};
+  int64_t grid = tiles < g_sms ? tiles : g_sms;
+  if (tiles % g_sms != 0 && nch >= 2 && a.ws && a.cnt) {
+    if (tiles > g_sms) {
+      sched.dp_tiles = (int)((tiles / g_sms - 1) * g_sms);
+      sched.usk = (tiles - sched.dp_tiles) * nch;
+      grid = g_sms;
+    } else {
+      const int64_t g = std::min<int64_t>(g_sms, tiles * nch / min_chunks);
+      if (g > tiles) {
+        sched.dp_tiles = 0;
+        sched.usk = tiles * nch;
+        grid = g;
+      }
+    }
+  }
   float* Y = a.Y;
+  float* ws = a.ws;
+  uint32_t* tcnt = a.cnt;
   int M = (int)a.M, N = (int)a.N, K = (int)a.K, ntv = nt, mt = (int)mtiles, ntl = (int)ntiles, gm = 8;
   uint32_t* err = a.err;
-  void* args[] = {&tmx, &tmw, &tmy, &tma_y, &Y, &M, &N, &K, &ntv, &mt, &ntl, &gm, &err};
+  void* args[] = {&tmx, &tmw, &tmy, &tma_y, &Y, &M, &N, &K, &ntv, &mt, &ntl, &gm, &sched, &ws, &tcnt, &err};
   return cudaLaunchKernel(tc_kernel(variant, act), dim3((unsigned)grid), dim3(kThreads), args, plan.smem, s);
 }
 

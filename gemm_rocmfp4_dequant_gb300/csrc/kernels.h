@@ -49,9 +49,13 @@ struct TcArgs {
   const uint16_t* X;
   float* Y;
   int64_t M, N, K, row_bytes;
+  float* ws;       // split-tile partials: tc_ws_floats(sms) floats
+  uint32_t* cnt;   // split-tile counters: tc_cnt_words(sms) words, zero between launches
   uint32_t* err;
 };
 int tc_k_multiple(int variant);   // 256 (dual) or 512 (single-scale)
+size_t tc_ws_floats(int sms);     // 2 partial tiles of 128 x 256 fp32 per SM
+size_t tc_cnt_words(int sms);     // one counter per tile of the split region (at most 2 per SM)
 cudaError_t tc_prepare();         // resolves cuTensorMapEncodeTiled, sets the smem attributes
 cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s);
 

@@ -159,3 +159,43 @@ def test_prefill_largest_batch_sampled():
 
 def test_prefill_fast_variant_and_fp16_sampled():
     prefill_case("o", 4096, variant=FAST, act=F16)
+
+
+# ---- K split across CTAs -----------------------------------------------------------------
+# Fewer tiles than SMs (or a partial last wave): each tile's K range is shared
+# by consecutive CTAs whose partial tiles the last one to finish adds in
+# chunk order.  One 128 x 16 tile over K = 8192 is cut into 8 parts; the
+# results must match the oracle, repeat bit for bit (fixed order), and stay
+# right on later launches (the hand-off counters reset themselves).
+
+@pytest.mark.parametrize("variant,M,N,K", [(DUAL, 16, 128, 8192), (DUAL, 33, 250, 17408),
+                                           (FAST, 20, 256, 16384), (DUAL, 600, 520, 4096)])
+def test_split_k_matches_oracle_and_repeats(variant, M, N, K):
+    t = torch()
+    Wh = synth.weights(N, K, variant, seed=16, stream=1700 + N)
+    Xh = synth.activations(M, K, BF16, seed=16, stream=1701)
+    W, X = upload_w(Wh), upload_x(Xh, BF16)
+    ref = oracle.gemm(Wh, Xh, N, K, variant, act=BF16)
+    first = None
+    for _ in range(3):
+        Y = rf4.gemm(W, X, N, K, variant)
+        assert_close(Y.cpu().numpy(), ref, K, max_halfscale(Wh, variant), f"split M={M} N={N} K={K}")
+        if first is None:
+            first = Y
+        else:
+            assert t.equal(first.view(t.int32), Y.view(t.int32))
+
+
+def test_split_k_shapes_interleaved():
+    """Split and unsplit launches back to back share the counters and workspace."""
+    shapes = [(DUAL, 16, 128, 8192), (DUAL, 300, 4096, 1024), (FAST, 40, 128, 4096), (DUAL, 64, 384, 2048)]
+    data = []
+    for i, (v, M, N, K) in enumerate(shapes):
+        Wh = synth.weights(N, K, v, seed=17, stream=1800 + i)
+        Xh = synth.activations(M, K, F16, seed=17, stream=1900 + i)
+        data.append((v, M, N, K, Wh, Xh, upload_w(Wh), upload_x(Xh, F16)))
+    for _ in range(2):
+        outs = [rf4.gemm(W, X, N, K, v) for v, M, N, K, _, _, W, X in data]
+        for (v, M, N, K, Wh, Xh, _, _), Y in zip(data, outs):
+            ref = oracle.gemm(Wh, Xh, N, K, v, act=F16)
+            assert_close(Y.cpu().numpy(), ref, K, max_halfscale(Wh, v), f"interleaved M={M} N={N} K={K}")
