@@ -511,6 +511,74 @@ def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True):
     return res
 
 
+# ---- fused gate/up GEMV -----------------------------------------------------------------------
+
+GATE_UP = (17408, 5120)  # I, K of the layer's gate+up matrix (2I = 34816 rows)
+
+
+def gate_up_bytes(I, K, variant=0, M=1):
+    """Algorithmic bytes of one fused gate/up product: 2I weight rows, M activation
+    rows in, M x I outputs."""
+    return matrix_bytes(2 * I, K, variant) + 2 * M * K + 4 * M * I
+
+
+def run_gate_up(hbm, reps=16):
+    """Fused gate/up product (Y = SiLU(gate . x) * (up . x)) on the layer's gate+up
+    matrix, batch 1, dual, x fp16: average device time per launch of a CUDA graph of
+    `reps` launches rotating over resident copies (every launch streams from HBM),
+    beside the plain GEMV of the same matrix (2I outputs, no epilogue)."""
+    import torch
+
+    import gemm_rocmfp4_dequant_gb300 as rf4
+    import synth
+    import synth.device
+    I, K = GATE_UP
+    copies = max(2, int(np.ceil(4 * L2_BYTES / matrix_bytes(2 * I, K))) + 1)
+    W, X, Yf, Yp = [], [], [], []
+    for r in range(copies):
+        w = torch.empty(2 * I * rf4.row_bytes(K, 0), dtype=torch.uint8, device="cuda")
+        synth.device.fill_weights(w, 2 * I, K, 0, seed=r, stream=synth.weight_stream(0, 2))
+        x = torch.empty((1, K), dtype=torch.int16, device="cuda")
+        synth.device.fill_act(x, 0, seed=r, stream=synth.act_stream(0, 2))
+        W.append(w)
+        X.append(x.view(torch.float16))
+        Yf.append(torch.empty((1, I), dtype=torch.float32, device="cuda"))
+        Yp.append(torch.empty((1, 2 * I), dtype=torch.float32, device="cuda"))
+    rf4.gemv_gate_up(W[0], X[0], I, K, 0, Y=Yf[0])
+    rf4.gemm(W[0], X[0], 2 * I, K, 0, Y=Yp[0])
+    torch.cuda.synchronize()
+
+    def per_launch(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fn(i % copies)
+        g.replay()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(5):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / (5 * reps)
+
+    launches0 = rf4.launch_count()
+    tf = per_launch(lambda r: rf4.gemv_gate_up(W[r], X[r], I, K, 0, Y=Yf[r]))
+    tp = per_launch(lambda r: rf4.gemm(W[r], X[r], 2 * I, K, 0, Y=Yp[r]))
+    assert rf4.launch_count() - launches0 == 2 * reps  # one launch per call while capturing
+    b = gate_up_bytes(I, K)
+    out = {"kernel": "gemv_stream_kernel, gate/up epilogue", "I": I, "K": K, "variant": "dual", "M": 1,
+           "act": "fp16", "us": round(tf * 1e6, 2), "GB/s": round(b / tf / 1e9, 1), "peak": hbm,
+           "frac": round(b / tf / 1e9 / hbm, 4), "algorithmic_bytes": b,
+           "plain_gemv_us": round(tp * 1e6, 2), "copies": copies,
+           "note": "plain_gemv_us: the same matrix as one GEMV of 2I outputs (SiLU*mul not applied)"}
+    del W, X, Yf, Yp
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---- prefill GEMM ---------------------------------------------------------------------------
 
 def run_prefill(Ms, tflops_peak, reps_small=10, reps_large=3):
@@ -763,6 +831,7 @@ def main():
         line["gpu_launches"] = res["gpu_launches"]
         line["clocks"] = res["clocks"]
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
+        line["gate_up"] = run_gate_up(hbm)
         if not args.no_prefill:
             pre, _ = run_prefill([int(m) for m in args.prefill_m.split(",")], bf16)
             line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16", "peak": bf16, "peak_kind": f"{peak_kind} bf16 burst",

@@ -25,7 +25,7 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
@@ -60,6 +60,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rocmfp4_gemm": ([vp, vp, vp, i64, i64, i64, c_int], c_int),
         "rocmfp4_gemm_ex": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemm_noalloc": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_gemv_gate_up": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
@@ -155,6 +156,25 @@ def gemv(W, x, N: int, K: int, variant: int = DUAL, y=None, stream=None):
     _check(load().rocmfp4_gemv_ex(_ptr(W), _ptr(x), _ptr(y), N, K, variant, _act_of(x), _stream(stream)),
            "rocmfp4_gemv_ex")
     return y
+
+
+def gemv_gate_up(W, X, I: int, K: int, variant: int = DUAL, Y=None, stream=None):
+    """Y[M, I] = SiLU(X . Wg^T) * (X . Wu^T) in fp32, where W packs 2I rows:
+    the I gate rows, then the I up rows (X fp16 or bf16 [M, K], M <= 8)."""
+    torch = _torch()
+    _check_w(W, 2 * I, K, variant)
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    if not X.is_cuda or not X.is_contiguous() or X.shape[1] != K:
+        raise ValueError("X must be a contiguous [M, K] CUDA tensor")
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, I), dtype=torch.float32, device=X.device)
+    elif Y.dtype != torch.float32 or not Y.is_contiguous() or Y.numel() < M * I:
+        raise ValueError("Y must be a contiguous float32 tensor with M*I elements")
+    _check(load().rocmfp4_gemv_gate_up(_ptr(W), _ptr(X), _ptr(Y), M, I, K, variant, _act_of(X), _stream(stream)),
+           "rocmfp4_gemv_gate_up")
+    return Y
 
 
 def gemv_chain(ops, variant: int = DUAL, stream=None):

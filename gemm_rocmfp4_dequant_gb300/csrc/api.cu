@@ -255,6 +255,56 @@ rocmfp4_status chain(const rocmfp4_gemv_op* ops, int count, int64_t M, int varia
   return ROCMFP4_OK;
 }
 
+// Fused gate/up product (M <= 8): W holds 2I rows, the I gate rows then the
+// I up rows; Y[m][i] = SiLU(gate_i . x_m) * (up_i . x_m).
+rocmfp4_status gate_up(const void* W, const void* X, float* Y, int64_t M, int64_t I, int64_t K, int variant, int act,
+                       cudaStream_t s) {
+  rocmfp4_status st = check_shape(I, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  if (!valid_act(act)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown activation type");
+  if (M < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  if (M == 0 || I == 0) return ROCMFP4_OK;
+  if (M > 8) return fail(ROCMFP4_ERR_UNSUPPORTED, "gate/up product: at most 8 activation rows");
+  if (Y == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "Y is NULL");
+  if (K > 0 && W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "W is NULL");
+  if (K == 0) {  // SiLU(0) * 0
+    cudaError_t e = cudaMemsetAsync(Y, 0, sizeof(float) * M * I, s);
+    return e == cudaSuccess ? ROCMFP4_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+  if (X == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "X is NULL");
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ROCMFP4_OK) return st;
+  const int64_t ku = stream_weights_per_unit(variant);
+  const int64_t nspans = K / ku;
+  const int64_t units = (I + kStreamTileRows / 2 - 1) / (kStreamTileRows / 2) * nspans;
+  if (K % ku != 0 || !aligned16(W) || !aligned16(X) || units >= (int64_t(1) << 31))
+    return fail(ROCMFP4_ERR_UNSUPPORTED,
+                "gate/up product: K must be a multiple of 256 (dual) or 512 (single-scale), W and X 16-byte aligned");
+  const int mb = stream_mb_for((int)M);
+  const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
+  const int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
+  GemvArgs a{};
+  a.W = static_cast<const uint8_t*>(W);
+  a.X = static_cast<const uint16_t*>(X);
+  a.Y = Y;
+  a.N = I;
+  a.K = K;
+  a.row_bytes = K / 32 * block_bytes_of(variant);
+  a.M = (int)M;
+  a.nspans = nspans;
+  a.units = units;
+  a.wact = units < cap ? units : cap;
+  a.ws = d->ws;
+  a.cnt = d->cnt;
+  a.err = d->err;
+  a.epi = 1;
+  const int ctas = (int)((a.wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
+  cudaError_t e = launch_gemv_stream(variant, act, a, ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
+  g_launches.fetch_add(1);
+  return ROCMFP4_OK;
+}
+
 }  // namespace
 
 namespace rocmfp4 {
@@ -291,6 +341,11 @@ rocmfp4_status rocmfp4_gemm(const void* W, const void* X, float* Y, int64_t M, i
 rocmfp4_status rocmfp4_gemm_ex(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
                                rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
   return product(W, X, Y, M, N, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rocmfp4_status rocmfp4_gemv_gate_up(const void* W, const void* X, float* Y, int64_t M, int64_t I, int64_t K,
+                                    rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
+  return gate_up(W, X, Y, M, I, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
 }
 
 rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op* ops, int count, int64_t M, rocmfp4_variant variant,

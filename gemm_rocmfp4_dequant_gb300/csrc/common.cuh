@@ -70,6 +70,16 @@ RF4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_
       : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared (box at element coordinates
+// (x, y, z)), completing the box's bytes on `bar`.
+RF4_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled tensor copy shared -> global of the box at (x, y); elements
 // outside the tensor are not written.  Part of the thread's bulk group.
 RF4_DEV void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {

@@ -131,13 +131,16 @@ RF4_DEV uint32_t weight_pair(uint32_t codes_f16x2, uint32_t s2) {
 // weight box (rows past N arrive as zeros) by lane 0, which also arms the
 // stage's barrier for the whole unit; then lanes 0..M-1 copy the unit's slice
 // of one activation row each (issue_x).
-template <int V, int MB>
+template <int V, int MB, int EPI>
 __device__ __forceinline__ void issue_w(const CUtensorMap* tmw, int M, int t, int j, uint8_t* stage, uint32_t bar,
                                         int lane) {
   using F = Fmt<V>;
   if (lane == 0) {
     mbar_arrive_expect_tx(bar, (uint32_t)(kTileRows * F::SPAN + M * F::KU * 2));
-    tma_load_2d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * kTileRows, bar);
+    if constexpr (EPI)  // box {span, 16 rows, gate and up halves}: gate rows land in rows 0-15, up rows in 16-31
+      tma_load_3d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * (kTileRows / 2), 0, bar);
+    else
+      tma_load_2d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * kTileRows, bar);
   }
 }
 
@@ -516,7 +519,28 @@ RF4_DEV void sum_records(const float* base, int64_t idx0, int64_t first, int64_t
   }
 }
 
-RF4_DEV void store_rows(float* __restrict__ Y, int64_t N, int64_t row, const float (&sum)[8], int M) {
+// SiLU(g) = g / (1 + exp(-g)) with the fast exponential and division (no
+// slow-path subroutine in the kernel): relative error a few 1e-6 where the
+// gate is not saturated; very negative g (exp(-g) = inf) gives 0.
+RF4_DEV float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Stores tile t from row-per-lane sums (lane r holds row r of the tile).  In
+// gate/up mode lanes 0-15 hold the gate rows and 16-31 the up rows of the
+// tile's 16 outputs.  Every lane of the warp must call it.
+template <int EPI>
+RF4_DEV void store_rows(float* __restrict__ Y, int64_t N, int64_t t, int lane, const float (&sum)[8], int M) {
+  if constexpr (EPI) {
+    float up[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) up[m] = __shfl_down_sync(0xffffffffu, sum[m], 16);
+    const int64_t o = t * (kTileRows / 2) + lane;
+    if (lane < 16 && o < N)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (m < M) Y[m * N + o] = silu(sum[m]) * up[m];
+    return;
+  }
+  const int64_t row = t * kTileRows + lane;
   if (row < N)
 #pragma unroll
     for (int m = 0; m < 8; ++m)
@@ -532,7 +556,7 @@ RF4_DEV uint32_t shared_add_acq_rel(uint32_t* p, uint32_t v) {
 // End of tile t of product op for this warp (its spans [js, j] are in acc):
 // store the tile if the warp covered all of it, else hand its partial to the
 // split-tile reduction.  Resets acc.
-template <int MB, int NOPS>
+template <int MB, int EPI, int NOPS>
 RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_t wg, int t, int js, int j, int lane,
                          float (&acc)[2][4], const CtaRed& red) {
   constexpr bool COL = MB == 1;
@@ -557,11 +581,23 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
       acc[mt][1] = acc[mt][3] = 0.f;
     }
   }
-  const int64_t row = (int64_t)t * kTileRows + lane;
   if (js == 0 && j == S - 1) {
     // the whole tile is this warp's
     const int c0 = COL ? 0 : 2 * c, c1 = COL ? 1 : 2 * c + 1;
-    if (!COL || c == 0) {
+    if constexpr (EPI) {
+      // m-tile 0 holds the gate rows, m-tile 1 the up rows of the same outputs
+      if (!COL || c == 0) {
+        const int64_t oa = (int64_t)t * (kTileRows / 2) + q, ob = oa + 8;
+        if (c0 < M) {
+          if (oa < N) Y[c0 * N + oa] = silu(acc[0][0]) * acc[1][0];
+          if (ob < N) Y[c0 * N + ob] = silu(acc[0][2]) * acc[1][2];
+        }
+        if (!COL && c1 < M) {
+          if (oa < N) Y[c1 * N + oa] = silu(acc[0][1]) * acc[1][1];
+          if (ob < N) Y[c1 * N + ob] = silu(acc[0][3]) * acc[1][3];
+        }
+      }
+    } else if (!COL || c == 0) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int64_t ra = (int64_t)t * kTileRows + mt * 16 + q, rb = ra + 8;
@@ -607,7 +643,7 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
       const int64_t me = wg / per, uf = wf / per, ul = wl / per;
       if (uf == ul) {
         // every part was in this CTA
-        store_rows(Y, N, row, sum, M);
+        store_rows<EPI>(Y, N, t, lane, sum, M);
       } else {
         // one record per contributor in global memory, counted per tile
         const int slot_uf = U * (uf * per) / wact < tS ? 1 : 0;
@@ -620,7 +656,7 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
         old = __shfl_sync(0xffffffffu, old, 0);  // lane 0's acquire is shared with the warp
         if ((int64_t)old == ul - uf) {
           sum_records<true, 8>(p.ws, 0, uf, ul, slot_uf, lane, M, sum);
-          store_rows(Y, N, row, sum, M);
+          store_rows<EPI>(Y, N, t, lane, sum, M);
           __syncwarp();
           if (lane == 0) store_relaxed_gpu(&p.cnt[uf], 0u);
         }
@@ -641,7 +677,8 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
 // first product, the preceding grid (programmatic dependent launch); for
 // product g > 0 of a chain, all warps' work on product g - 1 (grid barrier).
 // The barrier also makes the split-tile workspace free for the next product.
-template <int V, int ACT, int MB, int NOPS>
+// EPI = 1: the gate/up mode (single-product launches only).
+template <int V, int ACT, int MB, int NOPS, int EPI>
 __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
   using F = Fmt<V>;
   constexpr int NS = stages<V, MB>();
@@ -690,7 +727,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
   int iw = 0, ix = 0, readable = 0;
   auto issue_w_next = [&]() {
     const int st = iw % NS;
-    issue_w<V, MB>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
+    issue_w<V, MB, EPI>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
     const int g0 = cw.g;
     ++iw;
     cursor_next(cw, p, wg);
@@ -749,7 +786,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
       __syncwarp();
       fence_proxy_async();
       if (j == Si - 1 || k == nunits - 1) {
-        finish_tile<MB>(p, op, wg, t, js, j, lane, acc, red);
+        finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
         js = 0;
       }
       if (++j == Si) {
@@ -784,24 +821,30 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
 }
 
 // Kernel instance for (variant, activation type, staged activation rows,
-// single product or chain).
-template <int V, int ACT, int NOPS>
+// single product or chain, plain or gate/up).
+template <int V, int ACT, int NOPS, int EPI>
 const void* kernel_for_mb(int mb) {
   switch (mb) {
-    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS>);
-    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS>);
-    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS>);
-    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS>);
+    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS, EPI>);
+    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS, EPI>);
+    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS, EPI>);
+    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS, EPI>);
   }
 }
 
-const void* stream_kernel(int variant, int act, int mb, bool chain) {
-  if (chain) {
-    if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, kChainOps>(mb) : kernel_for_mb<0, 1, kChainOps>(mb);
-    return act == 0 ? kernel_for_mb<1, 0, kChainOps>(mb) : kernel_for_mb<1, 1, kChainOps>(mb);
+template <int EPI>
+const void* single_kernel(int variant, int act, int mb) {
+  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, 1, EPI>(mb) : kernel_for_mb<0, 1, 1, EPI>(mb);
+  return act == 0 ? kernel_for_mb<1, 0, 1, EPI>(mb) : kernel_for_mb<1, 1, 1, EPI>(mb);
+}
+
+// kind 0: single product, 1: chain, 2: single gate/up product.
+const void* stream_kernel(int variant, int act, int mb, int kind) {
+  if (kind == 1) {
+    if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, kChainOps, 0>(mb) : kernel_for_mb<0, 1, kChainOps, 0>(mb);
+    return act == 0 ? kernel_for_mb<1, 0, kChainOps, 0>(mb) : kernel_for_mb<1, 1, kChainOps, 0>(mb);
   }
-  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, 1>(mb) : kernel_for_mb<0, 1, 1>(mb);
-  return act == 0 ? kernel_for_mb<1, 0, 1>(mb) : kernel_for_mb<1, 1, 1>(mb);
+  return kind == 2 ? single_kernel<1>(variant, act, mb) : single_kernel<0>(variant, act, mb);
 }
 
 template <int V>
@@ -823,8 +866,8 @@ int stream_weights_per_unit(int variant) { return variant == 0 ? Fmt<0>::KU : Fm
 size_t stream_smem_bytes(int variant, int mb) { return variant == 0 ? smem_for_mb<0>(mb) : smem_for_mb<1>(mb); }
 
 cudaError_t stream_prepare(int variant, int act, int mb) {
-  for (int chain = 0; chain < 2; ++chain) {
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel(variant, act, mb, chain != 0),
+  for (int kind = 0; kind < 3; ++kind) {
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel(variant, act, mb, kind),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes(variant, mb));
     if (e != cudaSuccess) return e;
   }
@@ -834,10 +877,10 @@ cudaError_t stream_prepare(int variant, int act, int mb) {
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm) {
   // The chain instance must fit as many CTAs per SM (all of its CTAs are co-resident).
   int one = 0, chain = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&one, stream_kernel(variant, act, mb, false), kWarps * 32,
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&one, stream_kernel(variant, act, mb, 0), kWarps * 32,
                                                                 stream_smem_bytes(variant, mb));
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&chain, stream_kernel(variant, act, mb, true), kWarps * 32,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&chain, stream_kernel(variant, act, mb, 1), kWarps * 32,
                                                     stream_smem_bytes(variant, mb));
   if (e != cudaSuccess) return e;
   *ctas_per_sm = one < chain ? one : chain;
@@ -863,6 +906,17 @@ namespace {
 
 cudaError_t encode_weights(int variant, const GemvArgs& a, CUtensorMap* tmw) {
   const int span = variant == 0 ? Fmt<0>::SPAN : Fmt<1>::SPAN;
+  if (a.epi) {
+    // Gate/up pairing: words x N rows x {gate, up}; a box takes 16 rows of each.
+    cuuint64_t dims[3] = {(cuuint64_t)(a.row_bytes / 4), (cuuint64_t)a.N, 2};
+    cuuint64_t strides[2] = {(cuuint64_t)a.row_bytes, (cuuint64_t)(a.row_bytes * a.N)};
+    cuuint32_t box[3] = {(cuuint32_t)(span / 4), (cuuint32_t)(kTileRows / 2), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(a.W), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  }
   // Weights as a 2-D array of 32-bit words: row_bytes/4 columns, N rows.
   cuuint64_t dims[2] = {(cuuint64_t)(a.row_bytes / 4), (cuuint64_t)a.N};
   cuuint64_t strides[1] = {(cuuint64_t)a.row_bytes};
@@ -921,7 +975,7 @@ cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, false), args);
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, a.epi ? 2 : 0), args);
 }
 
 cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
@@ -944,7 +998,7 @@ cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nop
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, true), args);
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, 1), args);
 }
 
 }  // namespace rocmfp4

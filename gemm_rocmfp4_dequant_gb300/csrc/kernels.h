@@ -12,17 +12,18 @@ void count_launch();                              // one more kernel for rocmfp4
 
 // Streaming product Y[M][N] = X[M][K] . W[N][K]^T for M <= 8.
 struct GemvArgs {
-  const uint8_t* W;      // N x row_bytes packed blocks
+  const uint8_t* W;      // N x row_bytes packed blocks (2N rows, gate then up, when epi)
   const uint16_t* X;     // M x K activations (fp16 or bf16 bits)
   float* Y;              // M x N outputs
   int64_t N, K, row_bytes;
   int M;
   int64_t nspans;        // K / weights-per-unit
-  int64_t units;         // ceil(N/32) * nspans
+  int64_t units;         // ceil(N/32) * nspans, or ceil(N/16) * nspans when epi
   int64_t wact;          // active warps (<= units)
   float* ws;             // 2 * wact records of 32 x 8 floats
   uint32_t* cnt;         // wact counters, zero between calls
   uint32_t* err;         // error bits
+  int epi = 0;           // 1: Y = SiLU(gate rows . x) * (up rows . x)
 };
 
 constexpr int kStreamWarpsPerCta = 4;

@@ -113,6 +113,27 @@ rocmfp4_status rocmfp4_gemm_ex(const void *W, const void *X, float *Y, int64_t M
                                int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                rocmfp4_stream_t stream);
 
+/* Fused gate/up decode product (the "gemv_gate_up" decode matvec kernel type
+ * named in "Feasibility Report: Porting ROCmFP4 to Atlas", section "Kernel
+ * System"; the pages give no definition, and this is the plain reading for a
+ * gated MLP):
+ *
+ *   Y[m][i] = SiLU(g) * u,  g = sum_k Wg[i][k] X[m][k],  u = sum_k Wu[i][k] X[m][k],
+ *   SiLU(g) = g / (1 + exp(-g)),
+ *
+ * for i < I and m < M.  W is one packed matrix of 2I rows and K columns: rows
+ * 0 .. I-1 are the gate rows Wg, rows I .. 2I-1 the up rows Wu (each row
+ * K/32 blocks, as for every entry point).  X is M x K of type act
+ * (row-major), Y is M x I fp32 (row-major), overwritten; g and u accumulate in
+ * fp32 and never leave the kernel.
+ *   - M at most 8 (decode); M > 8 returns ROCMFP4_ERR_UNSUPPORTED.
+ *   - K a multiple of 256 (dual) or 512 (single-scale) and W and X 16-byte
+ *     aligned, else ROCMFP4_ERR_UNSUPPORTED; K == 0 writes zeros.
+ *   - Asynchronous on `stream`; arguments checked as for every entry point. */
+rocmfp4_status rocmfp4_gemv_gate_up(const void *W, const void *X, float *Y, int64_t M, int64_t I,
+                                    int64_t K, rocmfp4_variant variant, rocmfp4_act act,
+                                    rocmfp4_stream_t stream);
+
 /* One product of a chain: Y = X . W^T with the layouts of rocmfp4_gemm_ex
  * (X is M x K of the chain's activation type, Y is M x N fp32). */
 typedef struct rocmfp4_gemv_op {

@@ -71,6 +71,7 @@ def bind(path: str) -> ctypes.CDLL:
         "oracle_dequant": ([vp, i64, i64, c_int, vp], c_int),
         "oracle_validate": ([vp, i64, i64, c_int], i64),
         "oracle_gemm": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
+        "oracle_gemv_gate_up": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -171,3 +172,26 @@ def gemv(W, x_bits, N: int, K: int, variant: int, act: int = ACT_F16,
          nthreads: int | None = None, L=None) -> np.ndarray:
     """fp64 y[N] = W . x for one activation vector."""
     return gemm(W, np.asarray(x_bits).reshape(1, K), N, K, variant, act, nthreads, L)[0]
+
+
+def gemv_gate_up(W, X_bits, I: int, K: int, variant: int, act: int = ACT_F16,
+                 nthreads: int | None = None, L=None) -> np.ndarray:
+    """fp64 Y[M, I] = SiLU(X . Wg^T) * (X . Wu^T), W holding 2I rows (the gate
+    rows, then the up rows) and X given as fp16/bf16 bit patterns.  The formula
+    is reading R11 of the "gemv_gate_up" kernel type ("Kernel System" section
+    of the report); see the C source."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    if X.ndim == 1:
+        X = X.reshape(1, -1)
+    M = X.shape[0]
+    assert X.shape[1] == K, (X.shape, K)
+    assert W.size >= 2 * I * row_bytes(K, variant, L)
+    Y = np.empty((M, I), dtype=np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _L(L).oracle_gemv_gate_up(W.ctypes.data, X.ctypes.data, int(act), Y.ctypes.data, M, I, K,
+                                   int(variant), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_gemv_gate_up failed with {rc}")
+    return Y

@@ -213,3 +213,31 @@ int oracle_gemm(const uint8_t *W, const uint16_t *X, int act, double *Y, int64_t
   free(tid);
   return status;
 }
+
+/* Fused gate/up product, the "gemv_gate_up" decode kernel type named in the
+ * "Kernel System" section of the same report.  The report gives no formula;
+ * the reading taken (R11) is the gated MLP of a decoder layer:
+ *   W holds 2I rows, the I gate rows then the I up rows;
+ *   g = (gate rows) . x,  u = (up rows) . x,  y[i] = SiLU(g[i]) * u[i],
+ *   SiLU(g) = g / (1 + exp(-g)),
+ * all in fp64.  The two products are oracle_gemm's, in full. */
+static double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
+
+int oracle_gemv_gate_up(const uint8_t *W, const uint16_t *X, int act, double *Y, int64_t M,
+                        int64_t I, int64_t K, int variant, int nthreads) {
+  if (oracle_check_shape(I, K, variant) || M < 0) return -1;
+  double *gu = (double *)malloc(sizeof(double) * (size_t)(M * 2 * I > 0 ? M * 2 * I : 1));
+  if (!gu) return -3;
+  int status = oracle_gemm(W, X, act, gu, M, 2 * I, K, variant, nthreads);
+  if (status == 0) {
+    for (int64_t m = 0; m < M; ++m) {
+      for (int64_t i = 0; i < I; ++i) {
+        const double g = gu[m * 2 * I + i];
+        const double u = gu[m * 2 * I + I + i];
+        Y[m * I + i] = oracle_silu(g) * u;
+      }
+    }
+  }
+  free(gu);
+  return status;
+}

@@ -84,7 +84,7 @@ def pin_failures(L=None) -> list[str]:
             fails.append(name)
 
     for section in (_pin_tables, _pin_scales, _pin_blocks, _pin_activations, _pin_brute_force,
-                    _pin_validate):
+                    _pin_validate, _pin_gate_up):
         try:
             with np.errstate(invalid="ignore"):
                 section(check, L)
@@ -185,3 +185,63 @@ def _pin_validate(check, L):
         flat[4 * bb + off] = 0x7F
         flat[5 * bb + 16] = 0x80
         check(f"validate planted {var}/{off}", oracle.validate(W, N, K, var, L) == 4)
+
+
+def _gate_up_matrix(g_codes, u_codes, var):
+    """2 x 32 rows (one gate row, one up row), half-scales 1.0: weight j of a
+    row is Codebook10[code j] (codes for j < 16 only, the other half zero)."""
+    W = np.zeros((2, synth.block_bytes(var)), dtype=np.uint8)
+    for r, codes in enumerate((g_codes, u_codes)):
+        for j, q in enumerate(codes):
+            W[r, j] = q & 0xF
+    W[:, 16:] = 0x40  # E4M3 2.0: half-scale 1.0
+    return W
+
+
+def _pin_gate_up(check, L):
+    # 9. The fused gate/up product, reading R11: y = SiLU(g) * u with the gate
+    #    rows first.  Pinned by identities of the logistic function, not by
+    #    its formula: with u = 1,
+    #      y(g) - y(-g) = g            (SiLU(g) = g * s(g), s(g) + s(-g) = 1)
+    #      y(g) + y(-g) = g tanh(g/2)  (s(g) - s(-g) = tanh(g/2))
+    #    The second identity holds for the logistic s only (not for the
+    #    Gaussian CDF of GELU, nor for a sign-flipped exponent).
+    for var in (DUAL, FAST):
+        x = f16_bits(np.ones(32))
+        # one gate weight 2 (code 2) and up weights summing to 3 (code 3): y = 3 SiLU(2)
+        W = _gate_up_matrix([2], [3], var)
+        y = oracle.gemv_gate_up(W, x, 1, 32, var, L=L)[0, 0]
+        check(f"gate/up order {var}", abs(y - 3.0 * (1.0 + np.tanh(1.0))) < 1e-13)
+        # identities over gate sums g = -20 .. 20 in steps of 0.5 (x scales the code-1 weight)
+        gs = np.arange(-40, 41) * 0.5
+        W = _gate_up_matrix([1], [1], var)
+        odd, even = True, True
+        for g in gs[gs > 0]:
+            xp = f16_bits(np.r_[g, np.zeros(31)])
+            xn = f16_bits(np.r_[-g, np.zeros(31)])
+            # up row weight 1 * x = g as well, so divide it out: y / g = SiLU(+-g) / (+-g) * ...
+            yp = oracle.gemv_gate_up(W, xp, 1, 32, var, L=L)[0, 0] / g
+            yn = oracle.gemv_gate_up(W, xn, 1, 32, var, L=L)[0, 0] / -g
+            odd &= abs((yp - yn) - g) <= 1e-12 * max(1.0, g)
+            even &= abs((yp + yn) - g * np.tanh(g / 2)) <= 1e-12 * max(1.0, g)
+        check(f"gate/up odd part {var}", odd)
+        check(f"gate/up logistic even part {var}", even)
+        # saturation: SiLU(30) = 30 to 1e-12, SiLU(-30) ~ -3e-12
+        xp = f16_bits(np.r_[30.0, np.zeros(31)])
+        xn = f16_bits(np.r_[-30.0, np.zeros(31)])
+        yp = oracle.gemv_gate_up(W, xp, 1, 32, var, L=L)[0, 0]
+        yn = oracle.gemv_gate_up(W, xn, 1, 32, var, L=L)[0, 0]
+        check(f"gate/up saturation {var}", abs(yp / 900.0 - 1.0) < 1e-11 and abs(yn) < 1e-9)
+    # brute force: random blocks, M > 1 and I > 1, every sum exact in fp64;
+    # expected value through the tanh form of the identities above
+    rng = np.random.default_rng(8)
+    for var in (DUAL, FAST):
+        I, K, M = 3, 96, 2
+        W = synth.weights(2 * I, K, var, seed=4, stream=12)
+        X = f16_bits(rng.integers(-8, 9, size=(M, K)).astype(np.float64) * 0.25)
+        dense = oracle.dequant(W, 2 * I, K, var, L)
+        Xf = X.view(np.float16).astype(np.float64)
+        G, U = Xf @ dense[:I].T, Xf @ dense[I:].T
+        want = 0.5 * G * (1.0 + np.tanh(G / 2)) * U
+        got = oracle.gemv_gate_up(W, X, I, K, var, nthreads=2, L=L)
+        check(f"gate/up brute force {var}", got.shape == (M, I) and np.allclose(got, want, rtol=1e-13, atol=1e-13))

@@ -21,6 +21,14 @@ def test_layer_and_model_bytes():
     assert bench.matrix_bytes(7168, 5120, variant=1) == 7168 * 160 * 17
 
 
+def test_gate_up_bytes():
+    # the fused product reads the 2I x K matrix of the layer's gate+up, one x, writes I outputs
+    I, K = bench.GATE_UP
+    assert 2 * I == 34816
+    assert bench.gate_up_bytes(I, K) == 34816 * (K // 32) * 18 + 2 * K + 4 * I
+    assert bench.gate_up_bytes(I, K, M=4) == bench.matrix_bytes(2 * I, K) + 8 * K + 16 * I
+
+
 def test_traffic_record_needs_the_measured_source(tmp_path, monkeypatch):
     src = tmp_path / "gemv.cu"
     src.write_text("kernel v1\n")

@@ -39,6 +39,10 @@ MUTANTS = {
     "validate misses second scale": ("(variant == ORACLE_DUAL) ? 2 : 1;", "1;"),
     "0x7F accepted": ("return s < 0x7Fu;", "return s < 0x80u;"),
     "fast block 18 bytes": ("if (variant == ORACLE_FAST) return 17;", "if (variant == ORACLE_FAST) return 18;"),
+    "gate and up swapped": ("Y[m * I + i] = oracle_silu(g) * u;", "Y[m * I + i] = oracle_silu(u) * g;"),
+    "sigmoid of -g": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    "up read from the gate row": ("const double u = gu[m * 2 * I + I + i];", "const double u = gu[m * 2 * I + i];"),
+    "gate/up output transposed": ("Y[m * I + i] = oracle_silu(g) * u;", "Y[i * M + m] = oracle_silu(g) * u;"),
 }
 
 
