@@ -72,6 +72,7 @@ def bind(path: str) -> ctypes.CDLL:
         "oracle_validate": ([vp, i64, i64, c_int], i64),
         "oracle_gemm": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
         "oracle_gemv_gate_up": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
+        "oracle_decode_attention": ([vp, c_int, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_dbl, c_int], c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -195,3 +196,22 @@ def gemv_gate_up(W, X_bits, I: int, K: int, variant: int, act: int = ACT_F16,
     if rc != 0:
         raise ValueError(f"oracle_gemv_gate_up failed with {rc}")
     return Y
+
+
+def decode_attention(q_bits, Kc, Vc, lens, B: int, H: int, Hkv: int, D: int, Tmax: int, scale: float,
+                     variant: int, act: int = ACT_F16, L=None) -> np.ndarray:
+    """fp64 out[B, H, D] of single-token attention over a ROCmFP4 K/V cache
+    (reading R12; see the C source): q [B, H, D] as fp16/bf16 bits, Kc and Vc
+    [B, Hkv, Tmax] rows of D/32 blocks, lens [B] tokens per sequence."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16).reshape(B, H, D)
+    Kc = np.ascontiguousarray(Kc, dtype=np.uint8).reshape(-1)
+    Vc = np.ascontiguousarray(Vc, dtype=np.uint8).reshape(-1)
+    lens = np.ascontiguousarray(lens, dtype=np.int32).reshape(B)
+    need = B * Hkv * Tmax * row_bytes(D, variant, L)
+    assert Kc.size >= need and Vc.size >= need, (Kc.size, Vc.size, need)
+    out = np.empty((B, H, D), dtype=np.float64)
+    rc = _L(L).oracle_decode_attention(q.ctypes.data, int(act), Kc.ctypes.data, Vc.ctypes.data, lens.ctypes.data,
+                                       out.ctypes.data, B, H, Hkv, D, Tmax, float(scale), int(variant))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_attention failed with {rc}")
+    return out

@@ -84,7 +84,7 @@ def pin_failures(L=None) -> list[str]:
             fails.append(name)
 
     for section in (_pin_tables, _pin_scales, _pin_blocks, _pin_activations, _pin_brute_force,
-                    _pin_validate, _pin_gate_up):
+                    _pin_validate, _pin_gate_up, _pin_attention):
         try:
             with np.errstate(invalid="ignore"):
                 section(check, L)
@@ -245,3 +245,90 @@ def _pin_gate_up(check, L):
         want = 0.5 * G * (1.0 + np.tanh(G / 2)) * U
         got = oracle.gemv_gate_up(W, X, I, K, var, nthreads=2, L=L)
         check(f"gate/up brute force {var}", got.shape == (M, I) and np.allclose(got, want, rtol=1e-13, atol=1e-13))
+
+
+def _kv_rows(codes, var, scale_byte=0x40):
+    """Cache rows of D = 32 (one block each) from per-row code lists (weight j <
+    16 = Codebook10[code j]; the rest 0), half-scales 1.0 by default."""
+    bb = synth.block_bytes(var)
+    R = np.zeros((len(codes), bb), dtype=np.uint8)
+    for r, cs in enumerate(codes):
+        for j, q in enumerate(cs):
+            R[r, j] = q & 0xF
+        R[r, 16:] = scale_byte
+    return R
+
+
+def _pin_attention(check, L):
+    # 10. Decode attention over a ROCmFP4 K/V cache, reading R12.
+    for var in (DUAL, FAST):
+        D = 32
+        dense = lambda R: oracle.dequant(R, R.shape[0], D, var, L)
+        rng = np.random.default_rng(9)
+        # (a) one token: the output is its V row exactly, whatever q
+        K1 = _kv_rows([[3, 5, 9]], var)
+        V1 = synth.weights(1, D, var, seed=5, stream=13)
+        q = f16_bits(rng.integers(-4, 5, size=D) * 0.5)
+        out = oracle.decode_attention(q, K1, V1, [1], 1, 1, 1, D, 1, 0.25, var, L=L)
+        check(f"attn one token {var}", np.array_equal(out[0, 0], dense(V1)[0]))
+        # (b) equal keys: the mean of the V rows
+        T = 6
+        Kc = np.repeat(_kv_rows([[1, 2, 3, 4]], var), T, axis=0)
+        Vc = synth.weights(T, D, var, seed=5, stream=14)
+        out = oracle.decode_attention(q, Kc, Vc, [T], 1, 1, 1, D, T, 0.3, var, L=L)
+        check(f"attn equal keys {var}", np.allclose(out[0, 0], dense(Vc).mean(axis=0), rtol=1e-14, atol=1e-14))
+        # (c) a dominant key, even at huge scores (max subtracted before exp)
+        Kc = _kv_rows([[0], [7], [0], [0]], var)  # row 1: weight 0 = 10
+        qd = f16_bits(np.r_[64.0, np.zeros(D - 1)])  # score of row 1: 640 * scale
+        Vc = synth.weights(4, D, var, seed=5, stream=15)
+        out = oracle.decode_attention(qd, Kc, Vc, [4], 1, 1, 1, D, 4, 4.0, var, L=L)
+        check(f"attn dominant key {var}", np.all(np.isfinite(out)) and np.allclose(out[0, 0], dense(Vc)[1], rtol=1e-15, atol=1e-15))
+        # (d) two tokens: p0 = (1 + tanh((s0 - s1)/2)) / 2 with s1 = 0
+        Kc = _kv_rows([[1], [0]], var)  # s0 = scale * q[0]
+        q2 = f16_bits(np.r_[3.0, np.zeros(D - 1)])
+        Vc = synth.weights(2, D, var, seed=5, stream=16)
+        out = oracle.decode_attention(q2, Kc, Vc, [2], 1, 1, 1, D, 2, 0.5, var, L=L)
+        p0 = 0.5 * (1.0 + np.tanh(0.5 * 1.5))
+        Vd = dense(Vc)
+        check(f"attn two tokens {var}", np.allclose(out[0, 0], p0 * Vd[0] + (1 - p0) * Vd[1], rtol=1e-14, atol=1e-14))
+        # (e) grouped heads: H = 4 over Hkv = 2, one token each: head h reads KV head h // 2
+        Kc = _kv_rows([[1], [2]], var)
+        Vc = synth.weights(2, D, var, seed=5, stream=17)
+        q4 = f16_bits(rng.integers(-4, 5, size=(4, D)) * 0.5)
+        out = oracle.decode_attention(q4, Kc, Vc, [1], 1, 4, 2, D, 1, 0.25, var, L=L)
+        Vd = dense(Vc)
+        check(f"attn grouped heads {var}", all(np.array_equal(out[0, h], Vd[h // 2]) for h in range(4)))
+        # (f) lengths: rows past lens[b] are ignored, lens 0 gives zeros (B = 2, Tmax = 4)
+        Kc = synth.weights(8, D, var, seed=5, stream=18)
+        Vc = synth.weights(8, D, var, seed=5, stream=19)
+        qb = f16_bits(rng.integers(-4, 5, size=(2, D)) * 0.25)
+        out = oracle.decode_attention(qb, Kc, Vc, [3, 0], 2, 1, 1, D, 4, 0.2, var, L=L)
+        K2, V2 = Kc.copy(), Vc.copy()
+        K2[3] ^= 0x33
+        V2[3] ^= 0x55
+        out2 = oracle.decode_attention(qb, K2, V2, [3, 0], 2, 1, 1, D, 4, 0.2, var, L=L)
+        check(f"attn lengths {var}", np.array_equal(out, out2) and np.all(out[1] == 0) and np.any(out[0] != 0))
+        # (g) scale: a power-of-two scale equals that scaling of q (exact)
+        o1 = oracle.decode_attention(qb, Kc, Vc, [4, 4], 2, 1, 1, D, 4, 0.5, var, L=L)
+        qh = f16_bits(qb.view(np.float16).astype(np.float64) * 0.5)
+        o2 = oracle.decode_attention(qh, Kc, Vc, [4, 4], 2, 1, 1, D, 4, 1.0, var, L=L)
+        check(f"attn scale {var}", np.allclose(o1, o2, rtol=1e-15, atol=1e-15))
+    # (h) brute force: numpy softmax over dense rows, B = 2, H = 4, Hkv = 2, D = 64
+    rng = np.random.default_rng(10)
+    for var in (DUAL, FAST):
+        B, H, Hkv, D, Tmax = 2, 4, 2, 64, 5
+        lens = np.array([5, 3])
+        Kc = synth.weights(B * Hkv * Tmax, D, var, seed=6, stream=20)
+        Vc = synth.weights(B * Hkv * Tmax, D, var, seed=6, stream=21)
+        q = f16_bits(rng.integers(-8, 9, size=(B, H, D)) * 0.125)
+        out = oracle.decode_attention(q, Kc, Vc, lens, B, H, Hkv, D, Tmax, 0.125, var, L=L)
+        Kd = oracle.dequant(Kc, B * Hkv * Tmax, D, var, L).reshape(B, Hkv, Tmax, D)
+        Vd = oracle.dequant(Vc, B * Hkv * Tmax, D, var, L).reshape(B, Hkv, Tmax, D)
+        qf = q.view(np.float16).astype(np.float64)
+        ok = True
+        for b in range(B):
+            for h in range(H):
+                sc = 0.125 * Kd[b, h // 2, :lens[b]] @ qf[b, h]
+                w = np.exp(sc - sc.max())
+                ok &= np.allclose(out[b, h], (w @ Vd[b, h // 2, :lens[b]]) / w.sum(), rtol=1e-12, atol=1e-12)
+        check(f"attn brute force {var}", ok)

@@ -43,6 +43,12 @@ MUTANTS = {
     "sigmoid of -g": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
     "up read from the gate row": ("const double u = gu[m * 2 * I + I + i];", "const double u = gu[m * 2 * I + i];"),
     "gate/up output transposed": ("Y[m * I + i] = oracle_silu(g) * u;", "Y[i * M + m] = oracle_silu(g) * u;"),
+    "attention max not subtracted": ("const double p = exp(s[t] - smax);", "const double p = exp(s[t]);"),
+    "kv head by modulo": ("const int64_t hk = h / G;", "const int64_t hk = h % Hkv;"),
+    "lengths ignored": ("int64_t T = lens[b];", "int64_t T = Tmax;"),
+    "scale dropped": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "values read from K": ("oracle_dequant(Vc + ((b * Hkv + hk) * Tmax + t) * rb", "oracle_dequant(Kc + ((b * Hkv + hk) * Tmax + t) * rb"),
+    "denominator dropped": ("for (int64_t d = 0; d < D; ++d) o[d] /= denom;", "(void)denom;"),
 }
 
 
