@@ -579,6 +579,73 @@ def run_gate_up(hbm, reps=16):
     return out
 
 
+# ---- decode attention over a ROCmFP4 K/V cache ------------------------------------------------
+
+ATTN_HEADS = (40, 8, 128)  # query heads, KV heads, head dim of the layer (5120 = 40 x 128; 1024 KV = 8 x 128)
+ATTN_CASES = ((1, 32768), (16, 4096))  # (sequences, tokens each)
+
+
+def attention_bytes(B, T, H=40, Hkv=8, D=128, variant=0):
+    """Algorithmic bytes of one decode-attention call with every sequence T tokens
+    long: the K and V rows read once, q in, out written."""
+    return 2 * B * Hkv * T * (D // 32) * block_bytes(variant) + 2 * B * H * D + 4 * B * H * D
+
+
+def run_attention(hbm, reps=16):
+    """Decode attention (one query token per sequence, dual ROCmFP4 K/V, q fp16):
+    device time per call of a CUDA graph of `reps` calls rotating over resident
+    caches (every call streams its cache from HBM)."""
+    import torch
+
+    import gemm_rocmfp4_dequant_gb300 as rf4
+    import synth.device
+    H, Hkv, D = ATTN_HEADS
+    out = {}
+    for B, T in ATTN_CASES:
+        kv = B * Hkv * T * rf4.row_bytes(D, 0)
+        copies = max(2, int(np.ceil(4 * L2_BYTES / (2 * kv))) + 1)
+        Ks, Vs, Qs, Os = [], [], [], []
+        for r in range(copies):
+            k = torch.empty(kv, dtype=torch.uint8, device="cuda")
+            v = torch.empty(kv, dtype=torch.uint8, device="cuda")
+            synth.device.fill_weights(k, B * Hkv * T, D, 0, seed=r, stream=synth.weight_stream(0, 5))
+            synth.device.fill_weights(v, B * Hkv * T, D, 0, seed=r, stream=synth.weight_stream(0, 6))
+            q = torch.empty((B, H, D), dtype=torch.int16, device="cuda")
+            synth.device.fill_act(q, 0, seed=r, stream=synth.act_stream(0, 5))
+            Ks.append(k)
+            Vs.append(v)
+            Qs.append(q.view(torch.float16))
+            Os.append(torch.empty((B, H, D), dtype=torch.float32, device="cuda"))
+        lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        scale = 1.0 / np.sqrt(D)
+        rf4.decode_attention(Qs[0], Ks[0], Vs[0], lens, Hkv, T, scale, 0, out=Os[0])
+        torch.cuda.synchronize()
+        launches0 = rf4.launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                r = i % copies
+                rf4.decode_attention(Qs[r], Ks[r], Vs[r], lens, Hkv, T, scale, 0, out=Os[r])
+        per_call = (rf4.launch_count() - launches0) / reps
+        g.replay()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(5):
+            g.replay()
+        e1.record(st)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / (5 * reps)
+        b = attention_bytes(B, T, H, Hkv, D)
+        out[f"B={B} T={T}"] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+                               "algorithmic_bytes": b, "launches_per_call": per_call, "copies": copies}
+        del g, Ks, Vs, Qs, Os
+        torch.cuda.empty_cache()
+    return {"kernel": "attn_split_kernel + attn_combine_kernel", "heads": H, "kv_heads": Hkv, "head_dim": D,
+            "variant": "dual", "act": "fp16", "peak": hbm, "cases": out}
+
+
 # ---- prefill GEMM ---------------------------------------------------------------------------
 
 def run_prefill(Ms, tflops_peak, reps_small=10, reps_large=3):
@@ -832,6 +899,7 @@ def main():
         line["clocks"] = res["clocks"]
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
         line["gate_up"] = run_gate_up(hbm)
+        line["attention"] = run_attention(hbm)
         if not args.no_prefill:
             pre, _ = run_prefill([int(m) for m in args.prefill_m.split(",")], bf16)
             line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16", "peak": bf16, "peak_kind": f"{peak_kind} bf16 burst",

@@ -25,7 +25,7 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
@@ -61,6 +61,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rocmfp4_gemm_ex": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemm_noalloc": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemv_gate_up": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_decode_attention": ([vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, c_int, c_int, vp],
+                                     c_int),
         "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
@@ -175,6 +177,31 @@ def gemv_gate_up(W, X, I: int, K: int, variant: int = DUAL, Y=None, stream=None)
     _check(load().rocmfp4_gemv_gate_up(_ptr(W), _ptr(X), _ptr(Y), M, I, K, variant, _act_of(X), _stream(stream)),
            "rocmfp4_gemv_gate_up")
     return Y
+
+
+def decode_attention(q, K, V, lens, Hkv: int, Tmax: int, scale: float, variant: int = DUAL, out=None,
+                     stream=None):
+    """out[B, H, D] (fp32) of single-token attention over a ROCmFP4 K/V cache:
+    q [B, H, D] fp16 or bf16, K and V uint8 holding [B, Hkv, Tmax] rows of D/32
+    blocks, lens int32 [B] (tokens per sequence), all on the GPU."""
+    torch = _torch()
+    if q.dim() != 3 or not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [B, H, D] CUDA tensor")
+    B, H, D = q.shape
+    rb = row_bytes(D, variant)
+    for t, name in ((K, "K"), (V, "V")):
+        if not t.is_cuda or t.dtype != torch.uint8 or not t.is_contiguous() or t.numel() < B * Hkv * Tmax * rb:
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor of B*Hkv*Tmax rows")
+    if not lens.is_cuda or lens.dtype != torch.int32 or lens.numel() < B:
+        raise ValueError("lens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
+    elif out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < B * H * D:
+        raise ValueError("out must be a contiguous float32 tensor with B*H*D elements")
+    _check(load().rocmfp4_decode_attention(_ptr(q), _ptr(K), _ptr(V), _ptr(lens), _ptr(out), B, H, Hkv, D, Tmax,
+                                           float(scale), variant, _act_of(q), _stream(stream)),
+           "rocmfp4_decode_attention")
+    return out
 
 
 def gemv_chain(ops, variant: int = DUAL, stream=None):

@@ -24,6 +24,7 @@ struct DeviceState {
   uint32_t* gbar = nullptr;          // grid barrier counter of chained launches
   float* tcws = nullptr;             // tensor-core kernel: split-tile partials
   uint32_t* tccnt = nullptr;         // tensor-core kernel: split-tile counters
+  float* attn_ws = nullptr;          // decode attention: split partials
   unsigned long long* vfirst = nullptr;
 };
 
@@ -63,6 +64,7 @@ rocmfp4_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if ((e = stream_init_driver()) != cudaSuccess) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
     if ((e = tc_prepare()) != cudaSuccess) return cuda_fail(e, "tensor-core kernel set-up");
+    if ((e = attn_prepare()) != cudaSuccess) return cuda_fail(e, "attention kernel set-up");
     int best = 1;
     for (int v = 0; v < 2; ++v)
       for (int a = 0; a < 2; ++a)
@@ -86,6 +88,8 @@ rocmfp4_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(d.tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d.sms))) != cudaSuccess)
       return cuda_fail(e, "cudaMemset");
+    if ((e = cudaMalloc(&d.attn_ws, sizeof(float) * attn_ws_floats(d.sms))) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(d.err, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     d.ready = true;
@@ -305,6 +309,42 @@ rocmfp4_status gate_up(const void* W, const void* X, float* Y, int64_t M, int64_
   return ROCMFP4_OK;
 }
 
+rocmfp4_status decode_attention(const void* q, const void* K, const void* V, const int32_t* lens, float* out,
+                                int64_t B, int64_t H, int64_t Hkv, int64_t D, int64_t Tmax, float scale, int variant,
+                                int act, cudaStream_t s) {
+  if (!valid_variant(variant)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown variant");
+  if (!valid_act(act)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown activation type");
+  if (B < 0 || H < 0 || Hkv < 1 || D < 0 || Tmax < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative or zero size");
+  if (H % Hkv != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "H must be a multiple of Hkv");
+  if (D % 32 != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "D must be a multiple of 32");
+  if (B == 0 || H == 0) return ROCMFP4_OK;
+  if (out == nullptr || q == nullptr || lens == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "NULL pointer");
+  if (Tmax > 0 && (K == nullptr || V == nullptr)) return fail(ROCMFP4_ERR_INVALID_ARG, "NULL pointer");
+  if (D != 64 && D != 128) return fail(ROCMFP4_ERR_UNSUPPORTED, "decode attention: D must be 64 or 128");
+  if (H / Hkv > 8) return fail(ROCMFP4_ERR_UNSUPPORTED, "decode attention: at most 8 query heads per KV head");
+  if (Tmax % 32 != 0) return fail(ROCMFP4_ERR_UNSUPPORTED, "decode attention: Tmax must be a multiple of 32");
+  if (Tmax > 0 && (!aligned16(K) || !aligned16(V)))
+    return fail(ROCMFP4_ERR_UNSUPPORTED, "decode attention: K and V must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lens) & 3u) != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "lens misaligned");
+  if (B * H >= (int64_t(1) << 31) || B * Hkv * Tmax >= (int64_t(1) << 40) || Tmax >= (int64_t(1) << 31))
+    return fail(ROCMFP4_ERR_UNSUPPORTED, "decode attention: sizes too large");
+  if (!(scale == scale)) return fail(ROCMFP4_ERR_INVALID_ARG, "scale is NaN");
+  if (Tmax == 0) {  // no token anywhere: zeros
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * B * H * D, s);
+    return e == cudaSuccess ? ROCMFP4_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+  DeviceState* d = nullptr;
+  rocmfp4_status st = device_state(&d);
+  if (st != ROCMFP4_OK) return st;
+  AttnArgs a{static_cast<const uint16_t*>(q), static_cast<const uint8_t*>(K), static_cast<const uint8_t*>(V), lens,
+             out, d->attn_ws, B, H, Hkv, D, Tmax, scale, d->err};
+  int launches = 0;
+  cudaError_t e = launch_decode_attention(variant, act, a, d->sms, s, &launches);
+  g_launches.fetch_add((uint64_t)launches);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return ROCMFP4_OK;
+}
+
 }  // namespace
 
 namespace rocmfp4 {
@@ -346,6 +386,13 @@ rocmfp4_status rocmfp4_gemm_ex(const void* W, const void* X, float* Y, int64_t M
 rocmfp4_status rocmfp4_gemv_gate_up(const void* W, const void* X, float* Y, int64_t M, int64_t I, int64_t K,
                                     rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
   return gate_up(W, X, Y, M, I, K, variant, act, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rocmfp4_status rocmfp4_decode_attention(const void* q, const void* K, const void* V, const int32_t* lens, float* out,
+                                        int64_t B, int64_t H, int64_t Hkv, int64_t D, int64_t Tmax, float scale,
+                                        rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream) {
+  return decode_attention(q, K, V, lens, out, B, H, Hkv, D, Tmax, scale, variant, act,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op* ops, int count, int64_t M, rocmfp4_variant variant,
@@ -443,6 +490,7 @@ void rocmfp4_shutdown(void) {
     cudaFree(d.gbar);
     cudaFree(d.tcws);
     cudaFree(d.tccnt);
+    cudaFree(d.attn_ws);
     cudaFree(d.vfirst);
     d = DeviceState{};
   }

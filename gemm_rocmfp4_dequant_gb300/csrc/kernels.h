@@ -60,6 +60,26 @@ size_t tc_cnt_words(int sms);     // one counter per tile of the split region (a
 cudaError_t tc_prepare();         // resolves cuTensorMapEncodeTiled, sets the smem attributes
 cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s);
 
+// Decode attention over a ROCmFP4 K/V cache (attention.cu): q [B][H][D],
+// K and V [B][Hkv][Tmax] rows of D/32 blocks, lens [B], out [B][H][D] fp32.
+// D is 64 or 128, H / Hkv at most 8, Tmax a multiple of 32, K and V 16-byte
+// aligned.  One split launch, plus a combine launch when the cache is split.
+constexpr int kAttnMaxD = 128;
+struct AttnArgs {
+  const uint16_t* q;
+  const uint8_t* K;
+  const uint8_t* V;
+  const int32_t* lens;
+  float* out;
+  float* ws;  // attn_ws_floats(sms) floats
+  int64_t B, H, Hkv, D, Tmax;
+  float scale;
+  uint32_t* err;
+};
+size_t attn_ws_floats(int sms);
+cudaError_t attn_prepare();
+cudaError_t launch_decode_attention(int variant, int act, const AttnArgs& a, int sms, cudaStream_t s, int* launches);
+
 // Any K % 32 == 0, any alignment: one warp per (row, column chunk).
 struct GenericArgs {
   const uint8_t* W;

@@ -134,6 +134,34 @@ rocmfp4_status rocmfp4_gemv_gate_up(const void *W, const void *X, float *Y, int6
                                     int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                     rocmfp4_stream_t stream);
 
+/* Decode attention over a ROCmFP4 K/V cache (one query token per sequence):
+ * the "FlashAttention K/V cache optimization" item of "Feasibility Report:
+ * Porting ROCmFP4 to Atlas" (sections "Why AMD is Different from NVIDIA" and
+ * "Option 2"), which gives no formula; this is the plain reading:
+ *
+ *   s_t = scale * sum_d q[b][h][d] K[b][hk][t][d],   0 <= t < lens[b],
+ *   out[b][h][d] = sum_t exp(s_t - max s) V[b][hk][t][d] / sum_t exp(s_t - max s),
+ *   hk = h / (H / Hkv)  (grouped-query attention; Hkv = H is plain MHA).
+ *
+ *   - q     [B][H][D] of type act (row-major), device;
+ *   - K, V  [B][Hkv][Tmax] rows, each D/32 packed blocks of `variant`
+ *           (row_bytes = D/32 * block_bytes), device, 16-byte aligned;
+ *   - lens  [B] int32 on the device: tokens held by sequence b; values are
+ *           clamped to [0, Tmax]; rows at or past lens[b] are never used
+ *           (they need not hold valid blocks); a sequence with no token gives
+ *           zeros;
+ *   - out   [B][H][D] fp32, overwritten.
+ *   - D must be 64 or 128, H / Hkv at most 8, Tmax a multiple of 32, else
+ *     ROCMFP4_ERR_UNSUPPORTED.  Scores, softmax and the weighted sum are fp32;
+ *     results are bitwise repeatable for the same shapes on the same device.
+ *   - One or two kernel launches on `stream` (a combine launch when the cache
+ *     is split across CTAs); the split partials use the per-device workspace. */
+rocmfp4_status rocmfp4_decode_attention(const void *q, const void *K, const void *V,
+                                        const int32_t *lens, float *out, int64_t B, int64_t H,
+                                        int64_t Hkv, int64_t D, int64_t Tmax, float scale,
+                                        rocmfp4_variant variant, rocmfp4_act act,
+                                        rocmfp4_stream_t stream);
+
 /* One product of a chain: Y = X . W^T with the layouts of rocmfp4_gemm_ex
  * (X is M x K of the chain's activation type, Y is M x N fp32). */
 typedef struct rocmfp4_gemv_op {

@@ -29,6 +29,12 @@ def test_gate_up_bytes():
     assert bench.gate_up_bytes(I, K, M=4) == bench.matrix_bytes(2 * I, K) + 8 * K + 16 * I
 
 
+def test_attention_bytes():
+    # K and V rows of 4 dual blocks (72 B) per token and KV head, q fp16 in, out fp32
+    assert bench.attention_bytes(1, 32768) == 2 * 8 * 32768 * 72 + 2 * 40 * 128 + 4 * 40 * 128
+    assert bench.attention_bytes(16, 4096, variant=1) == 2 * 16 * 8 * 4096 * 68 + 6 * 16 * 40 * 128
+
+
 def test_traffic_record_needs_the_measured_source(tmp_path, monkeypatch):
     src = tmp_path / "gemv.cu"
     src.write_text("kernel v1\n")
