@@ -73,6 +73,7 @@ def bind(path: str) -> ctypes.CDLL:
         "oracle_gemm": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
         "oracle_gemv_gate_up": ([vp, vp, c_int, vp, i64, i64, i64, c_int, c_int], c_int),
         "oracle_decode_attention": ([vp, c_int, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_dbl, c_int], c_int),
+        "oracle_quantize": ([vp, c_int, vp, i64, i64, c_int], c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -215,3 +216,14 @@ def decode_attention(q_bits, Kc, Vc, lens, B: int, H: int, Hkv: int, D: int, Tma
     if rc != 0:
         raise ValueError(f"oracle_decode_attention failed with {rc}")
     return out
+
+
+def quantize(src_bits, N: int, K: int, variant: int, act: int = ACT_F16, L=None) -> np.ndarray:
+    """ROCmFP4 blocks [N, row_bytes] of fp16/bf16 values (bit patterns, [N, K]),
+    by the scale and rounding rules of reading R13 (see the C source)."""
+    X = np.ascontiguousarray(src_bits, dtype=np.uint16).reshape(N, K)
+    W = np.zeros((N, row_bytes(K, variant, L)), dtype=np.uint8)
+    rc = _L(L).oracle_quantize(X.ctypes.data, int(act), W.ctypes.data, N, K, int(variant))
+    if rc != 0:
+        raise ValueError(f"oracle_quantize failed with {rc}")
+    return W

@@ -84,7 +84,7 @@ def pin_failures(L=None) -> list[str]:
             fails.append(name)
 
     for section in (_pin_tables, _pin_scales, _pin_blocks, _pin_activations, _pin_brute_force,
-                    _pin_validate, _pin_gate_up, _pin_attention):
+                    _pin_validate, _pin_gate_up, _pin_attention, _pin_quantize):
         try:
             with np.errstate(invalid="ignore"):
                 section(check, L)
@@ -332,3 +332,65 @@ def _pin_attention(check, L):
                 w = np.exp(sc - sc.max())
                 ok &= np.allclose(out[b, h], (w @ Vd[b, h // 2, :lens[b]]) / w.sum(), rtol=1e-12, atol=1e-12)
         check(f"attn brute force {var}", ok)
+
+
+def _pin_quantize(check, L):
+    # 11. The quantiser, reading R13 (smallest covering scale, nearest Codebook10
+    #     magnitude, ties to the smaller).  Pinned by the decode (pinned above)
+    #     and by properties that follow from the rule, not by restating it.
+    rng = np.random.default_rng(11)
+    for var in (DUAL, FAST):
+        bb = synth.block_bytes(var)
+        ng = 2 if var == DUAL else 1
+        # (a) round trip: blocks whose every scale group holds a code of
+        #     magnitude 10 (so the group's scale is the covering one), no code 8
+        nblk = 64
+        W = np.zeros((nblk, bb), dtype=np.uint8)
+        codes = rng.choice(np.r_[0:8, 9:16], size=(nblk, 32))
+        for g in range(ng):
+            lo = g * (32 // ng)
+            codes[:, lo + rng.integers(0, 32 // ng)] = rng.choice([7, 15])
+        W[:, :16] = codes[:, :16] | (codes[:, 16:] << 4)
+        W[:, 16:] = rng.integers(0x01, 0x7F, size=(nblk, bb - 16))  # finite, nonzero scales
+        N, K = 8, nblk // 8 * 32
+        Wm = W.reshape(N, -1)
+        dense = oracle.dequant(Wm, N, K, var, L)
+        # codes up to 10 and half-scales from 2^-10 to 224: every value is exact in fp16
+        check(f"quant round trip {var}", np.array_equal(oracle.quantize(f16_bits(dense), N, K, var, L=L), Wm))
+        # (b) error bound and minimal scale on random fp16 input
+        x = (rng.standard_normal((16, 256)) * np.exp2(rng.integers(-12, 10, size=(16, 1)))).astype(np.float16)
+        Q = oracle.quantize(x.view(np.uint16), 16, 256, var, L=L)
+        back = oracle.dequant(Q, 16, 256, var, L).reshape(16, 8, ng, 32 // ng)
+        xs = x.astype(np.float64).reshape(16, 8, ng, 32 // ng)
+        sc = Q.reshape(16, 8, bb)[:, :, 16:16 + ng]
+        hs = np.vectorize(lambda e: oracle.halfscale(int(e), L))(sc)
+        below = np.vectorize(lambda e: oracle.ue4m3(int(e) - 1, L) if e > 0 else 0.0)(sc)
+        amax = np.abs(xs).max(axis=3)
+        check(f"quant error bound {var}", np.all(np.abs(back - xs) <= hs[..., None] * (1 + 1e-12)))
+        check(f"quant minimal scale {var}", np.all((5 * below < amax) | (sc == 0)) and np.all(10 * hs >= amax))
+        # (c) sign symmetry: -x flips the sign bit of every nonzero code, same scales
+        Qn = oracle.quantize((-x).view(np.uint16), 16, 256, var, L=L).reshape(16, 8, bb)
+        Qp = Q.reshape(16, 8, bb)
+        lo, hi = Qp[..., :16] & 0xF, Qp[..., :16] >> 4
+        flip = lambda c: np.where(c == 0, 0, c ^ 8)
+        check(f"quant sign {var}", np.array_equal(Qn[..., 16:], Qp[..., 16:]) and
+              np.array_equal(Qn[..., :16] & 0xF, flip(lo)) and np.array_equal(Qn[..., :16] >> 4, flip(hi)))
+        # (d) doubling the input adds one to every scale exponent, codes unchanged
+        xm = (rng.standard_normal((4, 256)) * 3).astype(np.float16)
+        Q1 = oracle.quantize(xm.view(np.uint16), 4, 256, var, L=L).reshape(4, 8, bb)
+        Q2 = oracle.quantize((xm * np.float16(2)).view(np.uint16), 4, 256, var, L=L).reshape(4, 8, bb)
+        check(f"quant doubling {var}", np.array_equal(Q2[..., :16], Q1[..., :16]) and
+              np.array_equal(Q2[..., 16:].astype(int), Q1[..., 16:].astype(int) + 8))
+        # (e) the tie rule: with half-scale 1 (group max 10), 5 -> 4, 7 -> 6, 9 -> 8, 0.5 -> 0, 5.5 -> 6
+        row = np.zeros(32)
+        row[[0, 1, 2, 3, 4, 5]] = [10, 5, 7, 9, 0.5, 5.5]
+        if var == DUAL:
+            row[16] = 10
+        Qt = oracle.quantize(f16_bits(row), 1, 32, var, L=L)[0]
+        check(f"quant ties {var}", list(Qt[:6] & 0xF) == [7, 4, 5, 6, 0, 5] and Qt[16] == 0x40)
+        # (f) saturation above 5 * 448 = 2240, and zero groups
+        row = np.zeros(32)
+        row[0], row[1] = 30000.0, -2240.0
+        Qs = oracle.quantize(f16_bits(row), 1, 32, var, L=L)[0]
+        zero_ok = (Qs[17] == 0 and np.all(Qs[:16] >> 4 == 0)) if var == DUAL else True
+        check(f"quant saturation {var}", Qs[16] == 0x7E and Qs[0] & 0xF == 7 and Qs[1] & 0xF == 15 and zero_ok)

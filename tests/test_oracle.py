@@ -49,6 +49,12 @@ MUTANTS = {
     "scale dropped": ("s[t] = scale * acc;", "s[t] = acc;"),
     "values read from K": ("oracle_dequant(Vc + ((b * Hkv + hk) * Tmax + t) * rb", "oracle_dequant(Kc + ((b * Hkv + hk) * Tmax + t) * rb"),
     "denominator dropped": ("for (int64_t d = 0; d < D; ++d) o[d] /= denom;", "(void)denom;"),
+    "quant ties to the larger": ("while (k < 7 && a > oracle_cb_mid[k] * hs) ++k;", "while (k < 7 && a >= oracle_cb_mid[k] * hs) ++k;"),
+    "quant scale one too large": ("if (5.0 * oracle_ue4m3_value(e) >= amax) return e;", "if (5.0 * oracle_ue4m3_value(e) > amax) return e;"),
+    "quant one scale for both halves": ("const int groups = variant == ORACLE_DUAL ? 2 : 1,", "const int groups = 1,"),
+    "quant sign dropped": ("return x < 0.0 ? 8u + k : k;", "return k;"),
+    "quant nibbles swapped": ("blk[j] = (uint8_t)(code[j] | (code[j + 16] << 4));", "blk[j] = (uint8_t)(code[j + 16] | (code[j] << 4));"),
+    "quant midpoint 4.5": ("{0.5, 1.5, 2.5, 3.5, 5.0, 7.0, 9.0}", "{0.5, 1.5, 2.5, 3.5, 4.5, 7.0, 9.0}"),
 }
 
 
