@@ -646,6 +646,49 @@ def run_attention(hbm, reps=16):
             "variant": "dual", "act": "fp16", "peak": hbm, "cases": out}
 
 
+# ---- quantiser -----------------------------------------------------------------------------------
+
+def quantize_bytes(N, K, variant=0):
+    """Algorithmic bytes of quantising N x K 16-bit values: read once, blocks written once."""
+    return 2 * N * K + matrix_bytes(N, K, variant)
+
+
+def run_quantize(hbm, reps=8):
+    """bf16 -> dual ROCmFP4 of the layer's gate+up matrix [34816, 5120]: device
+    time per call of a CUDA graph of `reps` calls over resident sources
+    (356 MB each, larger than L2)."""
+    import torch
+
+    import gemm_rocmfp4_dequant_gb300 as rf4
+    N, K = 34816, 5120
+    copies = 2
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    srcs = [torch.randn((N, K), dtype=torch.float32, device="cuda", generator=gen).to(torch.bfloat16)
+            for _ in range(copies)]
+    outs = [torch.empty(N * rf4.row_bytes(K, 0), dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    rf4.quantize(srcs[0], 0, W=outs[0])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            rf4.quantize(srcs[i % copies], 0, W=outs[i % copies])
+    g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(3):
+        g.replay()
+    e1.record(st)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / (3 * reps)
+    b = quantize_bytes(N, K)
+    del g, srcs, outs
+    torch.cuda.empty_cache()
+    return {"kernel": "quantize_kernel", "N": N, "K": K, "src": "bf16", "variant": "dual", "us": round(t * 1e6, 2),
+            "GB/s": round(b / t / 1e9, 1), "peak": hbm, "frac": round(b / t / 1e9 / hbm, 4), "algorithmic_bytes": b}
+
+
 # ---- prefill GEMM ---------------------------------------------------------------------------
 
 def run_prefill(Ms, tflops_peak, reps_small=10, reps_large=3):
@@ -900,6 +943,7 @@ def main():
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
         line["gate_up"] = run_gate_up(hbm)
         line["attention"] = run_attention(hbm)
+        line["quantize"] = run_quantize(hbm)
         if not args.no_prefill:
             pre, _ = run_prefill([int(m) for m in args.prefill_m.split(",")], bf16)
             line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16", "peak": bf16, "peak_kind": f"{peak_kind} bf16 burst",

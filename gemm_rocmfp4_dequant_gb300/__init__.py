@@ -25,7 +25,7 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_quantize", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
@@ -63,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rocmfp4_gemv_gate_up": ([vp, vp, vp, i64, i64, i64, c_int, c_int, vp], c_int),
         "rocmfp4_decode_attention": ([vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, c_int, c_int, vp],
                                      c_int),
+        "rocmfp4_quantize": ([vp, c_int, vp, i64, i64, c_int, vp], c_int),
         "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
@@ -222,6 +223,21 @@ def gemv_chain(ops, variant: int = DUAL, stream=None):
             raise ValueError(f"product {i}: Y must be a contiguous float32 tensor with M*N elements")
         arr[i] = GemvOp(W.data_ptr(), Xm.data_ptr(), Y.data_ptr(), N, K)
     _check(load().rocmfp4_gemv_chain(arr, len(ops), M, variant, act, _stream(stream)), "rocmfp4_gemv_chain")
+
+
+def quantize(src, variant: int = DUAL, W=None, stream=None):
+    """ROCmFP4 blocks (uint8, N * row_bytes) of a [N, K] float16 / bfloat16 CUDA tensor."""
+    torch = _torch()
+    if src.dim() != 2 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous [N, K] CUDA tensor")
+    N, K = src.shape
+    if W is None:
+        W = torch.empty(N * row_bytes(K, variant), dtype=torch.uint8, device=src.device)
+    elif W.dtype != torch.uint8 or not W.is_contiguous() or W.numel() < N * row_bytes(K, variant):
+        raise ValueError("W must be a contiguous uint8 tensor of N * row_bytes bytes")
+    _check(load().rocmfp4_quantize(_ptr(src), _act_of(src), _ptr(W), N, K, variant, _stream(stream)),
+           "rocmfp4_quantize")
+    return W
 
 
 def dequant(W, N: int, K: int, variant: int = DUAL, out_dtype=None, out=None, stream=None):

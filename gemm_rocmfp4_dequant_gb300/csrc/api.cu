@@ -417,6 +417,22 @@ rocmfp4_status rocmfp4_dequant(const void* W, void* out, rocmfp4_out_dtype out_d
   return ROCMFP4_OK;
 }
 
+rocmfp4_status rocmfp4_quantize(const void* src, rocmfp4_act src_type, void* W, int64_t N, int64_t K,
+                                rocmfp4_variant variant, rocmfp4_stream_t stream) {
+  rocmfp4_status st = check_shape(N, K, variant);
+  if (st != ROCMFP4_OK) return st;
+  if (!valid_act(src_type)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown source type");
+  const int64_t nblocks = N * (K / 32);
+  if (nblocks == 0) return ROCMFP4_OK;
+  if (src == nullptr || W == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(src) & 1u) != 0) return fail(ROCMFP4_ERR_INVALID_ARG, "src misaligned");
+  cudaError_t e = launch_quantize(variant, src_type, static_cast<const uint16_t*>(src), static_cast<uint8_t*>(W),
+                                  nblocks, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  g_launches.fetch_add(1);
+  return ROCMFP4_OK;
+}
+
 rocmfp4_status rocmfp4_validate(const void* W, int64_t N, int64_t K, rocmfp4_variant variant,
                                 int64_t* first_bad_block, rocmfp4_stream_t stream) {
   if (first_bad_block) *first_bad_block = -1;

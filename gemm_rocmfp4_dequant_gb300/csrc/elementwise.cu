@@ -116,6 +116,85 @@ __global__ void gemm_generic_kernel(const GenericArgs a, int act) {
   }
 }
 
+// ---- quantiser: fp16 / bf16 -> ROCmFP4, one thread per block --------------------
+// Scale groups are the two 16-weight halves (dual) or the whole block
+// (single-scale).  A group's scale byte is the smallest e <= 0x7E whose
+// half-scale covers its largest magnitude, 5 * E4M3(e) >= amax (0x7E when
+// none does; 0 for a group of zeros); each weight takes the nearest
+// Codebook10 magnitude, ties to the smaller, by comparing |x| with the
+// midpoints times the half-scale.  Every product and comparison is exact in
+// fp32.  Non-finite inputs count as 0.
+
+// E4M3 value of a scale byte (bit 7 clear), exact.
+RF4_DEV float ue4m3_f32(uint32_t e) {
+  const uint32_t E = (e >> 3) & 15u, M = e & 7u;
+  return E ? __uint_as_float(((E + 120u) << 23) | (M << 20)) : (float)M * (1.0f / 512.0f);
+}
+
+RF4_DEV uint32_t quant_scale(float amax) {
+  if (!(amax > 0.f)) return 0u;
+  if (5.f * ue4m3_f32(0x7Eu) < amax) return 0x7Eu;
+  uint32_t lo = 0, hi = 0x7E;
+  while (lo < hi) {  // E4M3 values increase with the byte
+    const uint32_t mid = (lo + hi) >> 1;
+    if (5.f * ue4m3_f32(mid) >= amax) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+RF4_DEV uint32_t quant_code(float x, float hs) {
+  const float a = fabsf(x);
+  const uint32_t k = (a > 0.5f * hs) + (a > 1.5f * hs) + (a > 2.5f * hs) + (a > 3.5f * hs) + (a > 5.f * hs) +
+                     (a > 7.f * hs) + (a > 9.f * hs);
+  return k == 0 ? 0u : (x < 0.f ? 8u + k : k);
+}
+
+template <int V>
+__global__ void quantize_kernel(const uint16_t* __restrict__ src, int act, uint8_t* __restrict__ W, int64_t nblocks,
+                                bool vec) {
+  using F = Fmt<V>;
+  for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    float x[32];
+    const uint16_t* s = src + blk * 32;
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = reinterpret_cast<const uint4*>(s)[q];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x[8 * q + 2 * k] = act_to_f32((uint16_t)(w[k] & 0xFFFFu), act);
+          x[8 * q + 2 * k + 1] = act_to_f32((uint16_t)(w[k] >> 16), act);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = act_to_f32(s[i], act);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = isfinite(x[i]) ? x[i] : 0.f;
+    constexpr int NG = V == 0 ? 2 : 1, GS = 32 / NG;
+    uint32_t code[32], sc[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = g * GS; i < (g + 1) * GS; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      sc[g] = quant_scale(amax);
+      const float hs = 0.5f * ue4m3_f32(sc[g]);
+#pragma unroll
+      for (int i = g * GS; i < (g + 1) * GS; ++i) code[i] = hs > 0.f ? quant_code(x[i], hs) : 0u;
+    }
+    uint8_t* out = W + blk * F::BB;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] = (uint8_t)(code[j] | (code[j + 16] << 4));  // byte j: weights j, j+16
+#pragma unroll
+    for (int g = 0; g < NG; ++g) out[16 + g] = (uint8_t)sc[g];
+  }
+}
+
 int grid_for(int64_t work, int threads) {
   int64_t g = (work + threads - 1) / threads;
   if (g > 152 * 32) g = 152 * 32;
@@ -149,6 +228,15 @@ cudaError_t launch_validate(int variant, const uint8_t* W, int64_t nblocks, unsi
   const int threads = 256, grid = grid_for(nblocks, threads);
   if (variant == 0) validate_kernel<0><<<grid, threads, 0, s>>>(W, nblocks, first);
   else validate_kernel<1><<<grid, threads, 0, s>>>(W, nblocks, first);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(int variant, int act, const uint16_t* src, uint8_t* W, int64_t nblocks, cudaStream_t s) {
+  if (nblocks == 0) return cudaSuccess;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int threads = 128, grid = grid_for(nblocks, threads);
+  if (variant == 0) quantize_kernel<0><<<grid, threads, 0, s>>>(src, act, W, nblocks, vec);
+  else quantize_kernel<1><<<grid, threads, 0, s>>>(src, act, W, nblocks, vec);
   return cudaGetLastError();
 }
 

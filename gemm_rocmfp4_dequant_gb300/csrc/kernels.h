@@ -95,6 +95,9 @@ cudaError_t launch_dequant(int variant, int out_dtype, const uint8_t* W, void* o
                            cudaStream_t s);
 
 // First block with a non-finite scale byte -> atomicMin into *first (init INT64_MAX).
+// Quantiser fp16 / bf16 (act 0 / 1) -> ROCmFP4 blocks, one thread per block
+// of 32 consecutive source values.
+cudaError_t launch_quantize(int variant, int act, const uint16_t* src, uint8_t* W, int64_t nblocks, cudaStream_t s);
 cudaError_t launch_validate(int variant, const uint8_t* W, int64_t nblocks, unsigned long long* first,
                             cudaStream_t s);
 

@@ -220,6 +220,25 @@ rocmfp4_status rocmfp4_gemm_noalloc(const void *W, const void *X, float *Y, int6
                                     int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                     rocmfp4_stream_t stream);
 
+/* Quantiser: packs src (N x K values of type src_type, row-major, device)
+ * into ROCmFP4 blocks W (N rows of K/32 blocks, device), the inverse of
+ * rocmfp4_dequant.  "Feasibility Report: Porting ROCmFP4 to Atlas", section
+ * "What is ROCmFP4?", defines the format but no scale selection or rounding;
+ * the rule used (a reading):
+ *   - scale groups: the two 16-weight halves of a dual block, the whole
+ *     block for single-scale;
+ *   - a group's scale byte e is the smallest of 0x00 .. 0x7E whose half-scale
+ *     covers the group's largest magnitude (5 * E4M3(e) >= amax); larger
+ *     magnitudes use 0x7E and saturate at code +-10; a group of zeros gets 0;
+ *   - each value takes the nearest Codebook10 magnitude times the half-scale,
+ *     a tie going to the smaller magnitude; zero is code 0; non-finite inputs
+ *     count as 0.
+ * Every decision is exact, so the result does not depend on the device.
+ * Values already of the form Codebook10[q] * hs(e) with a code of magnitude
+ * 10 in every group come back bit for bit.  Asynchronous on `stream`. */
+rocmfp4_status rocmfp4_quantize(const void *src, rocmfp4_act src_type, void *W, int64_t N, int64_t K,
+                                rocmfp4_variant variant, rocmfp4_stream_t stream);
+
 /* Dense weights: out[n*K + k] = Codebook10[q] * hs(e) for every weight,
  * written as fp32, bf16 or fp16.  Every value is exactly representable in
  * all three types, so the result is exact; code 8 gives +0. */

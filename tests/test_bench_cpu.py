@@ -35,6 +35,10 @@ def test_attention_bytes():
     assert bench.attention_bytes(16, 4096, variant=1) == 2 * 16 * 8 * 4096 * 68 + 6 * 16 * 40 * 128
 
 
+def test_quantize_bytes():
+    assert bench.quantize_bytes(34816, 5120) == 2 * 34816 * 5120 + 34816 * 160 * 18
+
+
 def test_traffic_record_needs_the_measured_source(tmp_path, monkeypatch):
     src = tmp_path / "gemv.cu"
     src.write_text("kernel v1\n")
