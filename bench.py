@@ -892,7 +892,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="layer", choices=["layer", "single", "sweep", "model", "prefill"])
+    ap.add_argument("--workload", default="layer",
+                    choices=["layer", "single", "sweep", "model", "prefill", "gate_up", "attention", "quantize"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill object out of the layer line")
     ap.add_argument("--prefill-m", type=str, default=",".join(str(m) for m in PREFILL_M),
@@ -915,6 +916,13 @@ def main():
         "prefill": {"workload": "W4A16 prefill GEMM, dual weights of the four layer shapes x X bf16 [M,K] ~ N(0,1), "
                                 "M in {512, 4096, 23552}", "act": "bf16",
                     "l2": "flushed (256 MB write) before every timed call"},
+        "gate_up": {"workload": "fused gate/up GEMV, [2 x 17408, 5120] dual, batch 1, x fp16 ~ N(0,1)",
+                    "l2": "rotating resident copies larger than 4 x L2"},
+        "attention": {"workload": "decode attention over a dual ROCmFP4 K/V cache, 40 heads / 8 KV heads / D 128, "
+                                  "1 x 32768 and 16 x 4096 tokens, q fp16 ~ N(0,1)",
+                      "l2": "rotating resident caches larger than 4 x L2"},
+        "quantize": {"workload": "quantiser bf16 [34816, 5120] ~ N(0,1) -> dual ROCmFP4",
+                     "l2": "two resident 356 MB sources, larger than L2"},
     }
     cfg = cfgs[args.workload]
 
@@ -974,6 +982,23 @@ def main():
         first = table["dual M=1"]
         line = base_line(args, world, first["GB/s"], "GB/s", 0.0, cfg, "f16")
         line["sweep"] = table
+    elif args.workload in ("gate_up", "attention", "quantize"):
+        launches0 = rf4.launch_count()
+        if args.workload == "gate_up":
+            r = run_gate_up(hbm)
+            v, ms = r["GB/s"], r["us"] / 1e3
+        elif args.workload == "attention":
+            r = run_attention(hbm)
+            head = r["cases"]["B=1 T=32768"]
+            v, ms = head["GB/s"], head["us"] / 1e3
+        else:
+            r = run_quantize(hbm)
+            v, ms = r["GB/s"], r["us"] / 1e3
+        line = base_line(args, world, v, "GB/s", ms, cfg, "f16" if args.workload != "quantize" else "bf16")
+        line["roofline"] = {"bound": "hbm", "achieved": v, "peak": hbm, "unit": "GB/s", "frac": round(v / hbm, 4),
+                            "traffic": None, "peak_kind": peak_kind}
+        line["detail"] = r
+        line["gpu_launches"] = rf4.launch_count() - launches0
     else:  # prefill
         Ms = [int(m) for m in args.prefill_m.split(",")]
         pre, launches = run_prefill(Ms, bf16)

@@ -90,12 +90,29 @@ RF4_DEV uint32_t lds_bytes4(uint32_t saddr) {
   return __funnelshift_r(lds32(a), lds32(a + 4), (saddr & 3u) * 8u);
 }
 
+// Four bytes at an address whose offset from a 4-byte boundary is al (0..3),
+// or not known (al = -1).  Called with al a constant after unrolling, so the
+// branches fold away.
+RF4_DEV uint32_t lds_bytes4_al(uint32_t saddr, int al) {
+  if (al == 0) return lds32(saddr);
+  if (al > 0) return __funnelshift_r(lds32(saddr - al), lds32(saddr - al + 4), 8 * al);
+  return lds_bytes4(saddr);
+}
+
+// Offset from a 4-byte boundary of byte `off` of a token row, when rows start
+// on 4-byte boundaries (every row length here is a multiple of 4 except the
+// single-scale rows of D = 64), else -1.
+template <int V, int D>
+RF4_HOSTDEV constexpr int row_align(int off) {
+  return (Fmt<V>::BB * (D / 32)) % 4 == 0 ? off % 4 : -1;
+}
+
 // Scale pair of a block as f16x2 E4M3 values: (scale of weights 0-15, scale
 // of weights 16-31); the single-scale variant repeats its one scale.
 template <int V>
-RF4_DEV uint32_t block_scales(uint32_t block_saddr) {
+RF4_DEV uint32_t block_scales(uint32_t block_saddr, int al) {
   const uint32_t a = block_saddr + 16;
-  const uint32_t w = lds32(a & ~3u) >> ((a & 3u) * 8u);
+  const uint32_t w = al >= 0 ? lds32(a - al) >> (8 * al) : lds32(a & ~3u) >> ((a & 3u) * 8u);
   if constexpr (V == 0) {
     return e4m3x2<0>(w & 0xFFFFu);  // two bytes, never straddling a word (even address)
   } else {
@@ -230,8 +247,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
 #pragma unroll
       for (int kb = 0; kb < F::NB; ++kb) {
         uint32_t va[4], vb[4];
-        decode4(lds_bytes4(ra + kb * F::BB + 4 * c), block_scales<V>(ra + kb * F::BB), va);
-        decode4(lds_bytes4(rb + kb * F::BB + 4 * c), block_scales<V>(rb + kb * F::BB), vb);
+        const int alc = row_align<V, D>(kb * F::BB), als = row_align<V, D>(kb * F::BB + 16);
+        decode4(lds_bytes4_al(ra + kb * F::BB + 4 * c, alc), block_scales<V>(ra + kb * F::BB, als), va);
+        decode4(lds_bytes4_al(rb + kb * F::BB + 4 * c, alc), block_scales<V>(rb + kb * F::BB, als), vb);
         if constexpr (ACT == 1) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -311,8 +329,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
 #pragma unroll
       for (int kb = 0; kb < F::NB; ++kb) {
         uint32_t va[4], vb[4];
-        decode4(lds_bytes4(ra + kb * F::BB + 4 * c), block_scales<V>(ra + kb * F::BB), va);
-        decode4(lds_bytes4(rb + kb * F::BB + 4 * c), block_scales<V>(rb + kb * F::BB), vb);
+        const int alc = row_align<V, D>(kb * F::BB), als = row_align<V, D>(kb * F::BB + 16);
+        decode4(lds_bytes4_al(ra + kb * F::BB + 4 * c, alc), block_scales<V>(ra + kb * F::BB, als), va);
+        decode4(lds_bytes4_al(rb + kb * F::BB + 4 * c, alc), block_scales<V>(rb + kb * F::BB, als), vb);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // tokens past the sequence: zeros (their rows are not data)
           va[k] = ta < T ? va[k] : 0u;

@@ -134,15 +134,19 @@ RF4_DEV float ue4m3_f32(uint32_t e) {
 RF4_DEV uint32_t quant_scale(float amax) {
   if (!(amax > 0.f)) return 0u;
   if (5.f * ue4m3_f32(0x7Eu) < amax) return 0x7Eu;
-  uint32_t lo = 0, hi = 0x7E;
-  while (lo < hi) {  // E4M3 values increase with the byte
+  uint32_t lo = 0, hi = 0x7E;  // E4M3 values increase with the byte: 7 halvings of [0, 0x7E]
+#pragma unroll
+  for (int it = 0; it < 7; ++it) {
     const uint32_t mid = (lo + hi) >> 1;
-    if (5.f * ue4m3_f32(mid) >= amax) hi = mid;
-    else lo = mid + 1;
+    const bool cover = 5.f * ue4m3_f32(mid) >= amax;
+    hi = cover ? mid : hi;
+    lo = cover ? lo : mid + 1;
   }
   return lo;
 }
 
+// Code of x for half-scale hs (hs > 0): the nearest Codebook10 magnitude, ties
+// to the smaller, sign in bit 3; zero is code 0.
 RF4_DEV uint32_t quant_code(float x, float hs) {
   const float a = fabsf(x);
   const uint32_t k = (a > 0.5f * hs) + (a > 1.5f * hs) + (a > 2.5f * hs) + (a > 3.5f * hs) + (a > 5.f * hs) +
@@ -150,48 +154,72 @@ RF4_DEV uint32_t quant_code(float x, float hs) {
   return k == 0 ? 0u : (x < 0.f ? 8u + k : k);
 }
 
-template <int V>
-__global__ void quantize_kernel(const uint16_t* __restrict__ src, int act, uint8_t* __restrict__ W, int64_t nblocks,
-                                bool vec) {
+// Source value of a 16-bit pattern; non-finite values count as 0.
+template <int ACT>
+RF4_DEV float quant_src(uint32_t bits) {
+  if constexpr (ACT == 0) {
+    return (bits & 0x7C00u) == 0x7C00u ? 0.f : __half2float(__ushort_as_half((uint16_t)bits));
+  } else {
+    return (bits & 0x7F80u) == 0x7F80u ? 0.f : __uint_as_float(bits << 16);
+  }
+}
+
+template <int V, int ACT>
+__global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __restrict__ W, int64_t nblocks, bool vec) {
   using F = Fmt<V>;
   for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks;
        blk += (int64_t)gridDim.x * blockDim.x) {
-    float x[32];
+    uint32_t w[16];  // w[i] = (value 2i, value 2i+1)
     const uint16_t* s = src + blk * 32;
     if (vec) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 v = reinterpret_cast<const uint4*>(s)[q];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          x[8 * q + 2 * k] = act_to_f32((uint16_t)(w[k] & 0xFFFFu), act);
-          x[8 * q + 2 * k + 1] = act_to_f32((uint16_t)(w[k] >> 16), act);
-        }
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = act_to_f32(s[i], act);
+      for (int i = 0; i < 16; ++i) w[i] = (uint32_t)s[2 * i] | ((uint32_t)s[2 * i + 1] << 16);
     }
+    // value i: w[i / 2] half i % 2; scale group 0 = values 0..15, group 1 = 16..31 (dual)
+    float am0 = 0.f, am1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = isfinite(x[i]) ? x[i] : 0.f;
-    constexpr int NG = V == 0 ? 2 : 1, GS = 32 / NG;
-    uint32_t code[32], sc[NG];
+    for (int i = 0; i < 16; ++i) {
+      const float lo = fabsf(quant_src<ACT>(w[i] & 0xFFFFu)), hi = fabsf(quant_src<ACT>(w[i] >> 16));
+      if (i < 8) am0 = fmaxf(am0, fmaxf(lo, hi));
+      else am1 = fmaxf(am1, fmaxf(lo, hi));
+    }
+    uint32_t e0, e1;
+    if constexpr (V == 0) {
+      e0 = quant_scale(am0);
+      e1 = quant_scale(am1);
+    } else {
+      e0 = e1 = quant_scale(fmaxf(am0, am1));
+    }
+    const float hs0 = 0.5f * ue4m3_f32(e0), hs1 = 0.5f * ue4m3_f32(e1);
+    // byte j: value j (low nibble, group 0) and value j + 16 (high nibble, group 1)
+    uint32_t bytes[16];
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      float amax = 0.f;
-#pragma unroll
-      for (int i = g * GS; i < (g + 1) * GS; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      sc[g] = quant_scale(amax);
-      const float hs = 0.5f * ue4m3_f32(sc[g]);
-#pragma unroll
-      for (int i = g * GS; i < (g + 1) * GS; ++i) code[i] = hs > 0.f ? quant_code(x[i], hs) : 0u;
+    for (int j = 0; j < 16; ++j) {
+      const float xl = quant_src<ACT>((w[j / 2] >> (16 * (j % 2))) & 0xFFFFu);
+      const float xh = quant_src<ACT>((w[8 + j / 2] >> (16 * (j % 2))) & 0xFFFFu);
+      const uint32_t cl = hs0 > 0.f ? quant_code(xl, hs0) : 0u, ch = hs1 > 0.f ? quant_code(xh, hs1) : 0u;
+      bytes[j] = cl | (ch << 4);
     }
     uint8_t* out = W + blk * F::BB;
+    if constexpr (V == 0) {  // 18-byte blocks start on even addresses: nine 16-bit stores
+      uint16_t* o16 = reinterpret_cast<uint16_t*>(out);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) out[j] = (uint8_t)(code[j] | (code[j + 16] << 4));  // byte j: weights j, j+16
+      for (int k = 0; k < 8; ++k) o16[k] = (uint16_t)(bytes[2 * k] | (bytes[2 * k + 1] << 8));
+      o16[8] = (uint16_t)(e0 | (e1 << 8));
+    } else {
 #pragma unroll
-    for (int g = 0; g < NG; ++g) out[16 + g] = (uint8_t)sc[g];
+      for (int j = 0; j < 16; ++j) out[j] = (uint8_t)bytes[j];
+      out[16] = (uint8_t)e0;
+    }
   }
 }
 
@@ -235,8 +263,13 @@ cudaError_t launch_quantize(int variant, int act, const uint16_t* src, uint8_t* 
   if (nblocks == 0) return cudaSuccess;
   const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
   const int threads = 128, grid = grid_for(nblocks, threads);
-  if (variant == 0) quantize_kernel<0><<<grid, threads, 0, s>>>(src, act, W, nblocks, vec);
-  else quantize_kernel<1><<<grid, threads, 0, s>>>(src, act, W, nblocks, vec);
+  if (variant == 0) {
+    if (act == 0) quantize_kernel<0, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+    else quantize_kernel<0, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+  } else {
+    if (act == 0) quantize_kernel<1, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+    else quantize_kernel<1, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+  }
   return cudaGetLastError();
 }
 
