@@ -235,6 +235,21 @@ RF4_DEV void store_fix16(const float4 (&s4)[4], float* Y, int M, int N, int m, i
     if (m + j < M) Y[(size_t)(m + j) * N + n] = v[j];
 }
 
+// Waits (bounded: about two seconds of SM clock, acquire) until the written
+// half of a split-tile counter reaches `need`; false if it gave up.  The
+// writers wait on nothing of the waiting CTA's, and a grid with split tiles
+// is launched cooperatively, so every writer is resident.
+RF4_DEV bool wait_parts_written(uint32_t* cnt, uint32_t need) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if ((v >> 16) >= need) return true;
+    if (clock64() - t0 > (1ll << 32)) return false;
+    __nanosleep(32);
+  }
+}
+
 RF4_DEV Parts tile_parts(const Sched& sc, const float* ws, int t) {
   const int64_t t0 = (int64_t)(t - sc.dp_tiles) * sc.nch;
   Parts p;
@@ -510,10 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.accfree = b.cfree + 1;
   b.fixbar = b.accfree + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 1);
-  // Split tiles whose last part this CTA finished (at most two: a CTA's
-  // split range has a part at each end), summed by all threads after the
-  // roles end: {count, then (tile, m0, n0) per tile}.
+  // Split tiles whose last arrival was this CTA's (at most two: a CTA's split
+  // range has a part at each end), summed by all threads after the roles
+  // end: {count, then (tile, m0, n0, own part index or -1, own chains) per tile}.
   volatile int* fix = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* keep_flag = fix + 11;  // the output warps' count-first verdict
+  volatile int* wait_flag = fix + 12;  // the fix-up's wait for written parts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Raster raster{mtiles, ntiles, group_m, nt};
@@ -687,6 +704,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* part = whole ? nullptr
                           : ws + (size_t)(2 * blockIdx.x + (t0 + w.cb == sched.start((int)blockIdx.x) ? 0 : 1)) *
                                      kSlotFloats;
+      ItemIter peek = it;
+      Item nw;
+      const bool final_item = !peek.next(sched, nw);
+      const int bfirst = whole ? 0 : sched.owner(t0);
+      const int nparts = whole ? 1 : sched.owner(t0 + sched.nch - 1) - bfirst + 1;
+      bool keep = false;
       for (int c = nchains > 1 ? 1 : 0; c < nchains; ++c) {  // chain 0 of several stays in R
         // the four output warps leave together, so their named barriers stay matched
         if (!(ok = epi_all(warp_wait(smem_addr(b.cfull), (n_cfull++) & 1u)))) break;
@@ -707,6 +730,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(smem_addr(b.cfree));
           continue;
+        }
+        if (!whole && final_item) {
+          // Count first: if this arrival completes the tile, the part stays
+          // in tensor memory for the fix-up (low half of the counter:
+          // arrivals, high half: parts written).
+          if (row == 0) {
+            const uint32_t old = atomicAdd(&tcnt[w.t - sched.dp_tiles], 1u);
+            *keep_flag = (int)((old & 0xFFFFu) + 1u == (uint32_t)nparts);
+          }
+          epi_bar_sync();
+          keep = *keep_flag != 0;
+          if (keep && row == 0) {
+            const int i = fix[0];
+            fix[1 + 5 * i] = w.t;
+            fix[2 + 5 * i] = m0;
+            fix[3 + 5 * i] = n0;
+            fix[4 + 5 * i] = (int)blockIdx.x - bfirst;
+            fix[5 + 5 * i] = nchains;
+            fix[0] = i + 1;
+          }
+          if (keep) break;
         }
         // last chain: R (+ C), 16 tokens at a time, to Y or to the workspace
 #pragma unroll 1
@@ -734,22 +778,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok || whole) continue;
-      // Split tile: count the finished parts.  The CTA that finishes the last
-      // one adds all parts in chunk order (a fixed order, whichever CTA it
-      // is) once its roles have ended.  Nothing waits on another CTA.
-      const int nparts = tile_parts(sched, ws, w.t).nparts;
+      if (!ok || whole || keep) continue;
+      // Split tile, part written: publish it (and count the arrival too,
+      // unless the final item counted first).  The arrival that completes
+      // the tile records it; its CTA adds the parts in chunk order once its
+      // roles have ended, after waiting for every part to be written (each
+      // counted part is written by a CTA that waits on nothing meanwhile).
       epi_bar_sync();  // every output thread's part stores precede the count
       if (row == 0) {
         __threadfence();  // this CTA's part is visible before the count
-        const uint32_t done = atomicAdd(&tcnt[w.t - sched.dp_tiles], 1u) + 1u;
-        if (done == (uint32_t)nparts) {
-          __threadfence();                              // the other parts are visible after the count
-          atomicExch(&tcnt[w.t - sched.dp_tiles], 0u);  // ready for the next launch
+        const uint32_t old = atomicAdd(&tcnt[w.t - sched.dp_tiles], final_item ? 0x10000u : 0x10001u);
+        if (!final_item && (old & 0xFFFFu) + 1u == (uint32_t)nparts) {
           const int i = fix[0];
-          fix[1 + 3 * i] = w.t;
-          fix[2 + 3 * i] = m0;
-          fix[3 + 3 * i] = n0;
+          fix[1 + 5 * i] = w.t;
+          fix[2 + 5 * i] = m0;
+          fix[3 + 5 * i] = n0;
+          fix[4 + 5 * i] = -1;
+          fix[5 + 5 * i] = 0;
           fix[0] = i + 1;
         }
       }
@@ -760,74 +805,124 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(plan.tmem_cols));
-  }
-  // ---- split fix-up: all threads, shared memory free of the main loop ----
+  // ---- split fix-up: all threads; the stage and raw rings are free ----
+  // For each recorded tile: wait until every other part is written, bring
+  // those parts into shared memory by bulk copies (window by window), and
+  // add all parts in chunk order; this CTA's own part, when its final item
+  // counted first, is read from tensor memory (R + C, as it would have been
+  // written).  Tensor memory is released after the last fix-up.
+  tc_fence_after();
   const int nfix = fix[0];
   uint32_t fix_phase = 0;
   bool fix_ok = true;
+  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
 #pragma unroll 1
   for (int f = 0; f < nfix; ++f) {
-    const Parts parts = tile_parts(sched, ws, fix[1 + 3 * f]);
-    const int m0 = fix[2 + 3 * f], n0 = fix[3 + 3 * f];
-    const int groups = nt / 16;
-    constexpr uint32_t kGroupBytes = kTcRows * 16 * 4;  // one part, 16 tokens
-    // token groups per window: every part's window fits in the stage and raw rings
-    const int win = min(groups, (int)(plan.off_epi / ((uint32_t)parts.nparts * kGroupBytes)));
-    if (win == 0) {
-      // too many parts for shared memory: sum straight from the workspace
-#pragma unroll 1
-      for (int pi = threadIdx.x; pi < kTcRows * groups; pi += kThreads) {
-        const int row = pi % kTcRows, g = pi / kTcRows;
-        float4 s4[4];
-        parts.sum(g, row, s4);
-        store_fix16(s4, Y, M, N, m0 + 16 * g, n0 + row);
-      }
+    const int t = fix[1 + 5 * f], m0 = fix[2 + 5 * f], n0 = fix[3 + 5 * f];
+    const int own = fix[4 + 5 * f], nch_own = fix[5 + 5 * f];
+    const Parts parts = tile_parts(sched, ws, t);
+    const int ncopy = parts.nparts - (own >= 0 ? 1 : 0);
+    if (threadIdx.x == 0) {
+      uint32_t* cnt = &tcnt[t - sched.dp_tiles];
+      const bool okw = wait_parts_written(cnt, (uint32_t)ncopy);
+      if (okw) atomicExch(cnt, 0u);  // every contributor is done with it: ready for the next launch
+      *wait_flag = okw ? 1 : 0;
+    }
+    __syncthreads();
+    if (*wait_flag == 0) {
+      fix_ok = false;
+      __syncthreads();  // every thread has read the flag before thread 0 writes it again
       continue;
     }
+    const int groups = nt / 16;
+    constexpr uint32_t kGroupBytes = kTcRows * 16 * 4;  // one part, 16 tokens
+    // token groups per window: every copied part's window fits in the rings
+    const int win = ncopy == 0 ? groups : min(groups, (int)(plan.off_epi / ((uint32_t)ncopy * kGroupBytes)));
+    const bool from_ws = win == 0;  // too many parts for shared memory: read them in place
+    const int step = from_ws ? 1 : win;
 #pragma unroll 1
-    for (int g0 = 0; g0 < groups; g0 += win) {
-      const int gw = min(win, groups - g0);
+    for (int g0 = 0; g0 < groups; g0 += step) {
+      const int gw = min(step, groups - g0);
       const uint32_t pbytes = (uint32_t)gw * kGroupBytes;
-      if (threadIdx.x == 0) {
-        // the rings' last generic-proxy accesses, and the parts acquired
-        // through the counter, come before the bulk copies
-        asm volatile("fence.proxy.async;" ::: "memory");
-        mbar_arrive_expect_tx(smem_addr(b.fixbar), pbytes * (uint32_t)parts.nparts);
-        for (int k = 0; k < parts.nparts; ++k)
-          bulk_g2s(smem_addr(smem + (size_t)k * pbytes), parts.slot(k) + (size_t)g0 * kTcRows * 16, pbytes,
-                   smem_addr(b.fixbar));
+      if (!from_ws && ncopy > 0) {
+        if (threadIdx.x == 0) {
+          // the rings' last generic-proxy accesses, and the parts acquired
+          // through the counter, come before the bulk copies
+          asm volatile("fence.proxy.async;" ::: "memory");
+          mbar_arrive_expect_tx(smem_addr(b.fixbar), pbytes * (uint32_t)ncopy);
+          for (int k = 0, sk = 0; k < parts.nparts; ++k) {
+            if (k == own) continue;
+            bulk_g2s(smem_addr(smem + (size_t)sk * pbytes), parts.slot(k) + (size_t)g0 * kTcRows * 16, pbytes,
+                     smem_addr(b.fixbar));
+            ++sk;
+          }
+        }
+        fix_ok = mbar_wait_bounded(smem_addr(b.fixbar), fix_phase) && fix_ok;
+        fix_phase ^= 1u;
       }
-      fix_ok = mbar_wait_bounded(smem_addr(b.fixbar), fix_phase) && fix_ok;
-      fix_phase ^= 1u;
+      // (row, group) pairs: a warp's lanes are 32 rows of its tensor-memory
+      // lane quarter and share one group, as the tensor-memory loads need
 #pragma unroll 1
       for (int pi = threadIdx.x; pi < kTcRows * gw; pi += kThreads) {
-        const int row = pi % kTcRows, gl = pi / kTcRows;
+        const int row = pi % kTcRows, gl = pi / kTcRows, g = g0 + gl;
+        float4 own4[4];
+        if (own >= 0) {
+          uint32_t a[16], v[16];
+          tmem_ld16(tlane + (uint32_t)(16 * g), a);
+          if (nch_own > 1) tmem_ld16(tlane + plan.cstride + (uint32_t)(16 * g), v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (nch_own > 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(v[j]));
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            own4[q] = make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
+                                  __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3]));
+        }
         float4 s4[4];
 #pragma unroll 1
-        for (int k = 0; k < parts.nparts; ++k) {
-          const float4* src = reinterpret_cast<const float4*>(smem + (size_t)k * pbytes) + (size_t)gl * 4 * kTcRows + row;
+        for (int k = 0, sk = 0; k < parts.nparts; ++k) {
+          float4 v4[4];
+          if (k == own) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v4[q] = own4[q];
+          } else if (from_ws) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              v4[q] = __ldcg(reinterpret_cast<const float4*>(parts.slot(k) + part_index(g, q, row)));
+            ++sk;
+          } else {
+            const float4* src =
+                reinterpret_cast<const float4*>(smem + (size_t)sk * pbytes) + (size_t)gl * 4 * kTcRows + row;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v4[q] = src[q * kTcRows];
+            ++sk;
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 v = src[q * kTcRows];
             if (k == 0) {
-              s4[q] = v;
+              s4[q] = v4[q];
             } else {
-              s4[q].x += v.x;
-              s4[q].y += v.y;
-              s4[q].z += v.z;
-              s4[q].w += v.w;
+              s4[q].x += v4[q].x;
+              s4[q].y += v4[q].y;
+              s4[q].z += v4[q].z;
+              s4[q].w += v4[q].w;
             }
           }
         }
-        store_fix16(s4, Y, M, N, m0 + 16 * (g0 + gl), n0 + row);
+        store_fix16(s4, Y, M, N, m0 + 16 * g, n0 + row);
       }
       __syncthreads();  // the window is consumed before the next copies overwrite it
     }
   }
   if (!fix_ok) atomicOr(err, kErrWaitTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(plan.tmem_cols));
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -946,7 +1041,19 @@ cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s
   int M = (int)a.M, N = (int)a.N, K = (int)a.K, ntv = nt, mt = (int)mtiles, ntl = (int)ntiles, gm = 8;
   uint32_t* err = a.err;
   void* args[] = {&tmx, &tmw, &tmy, &tma_y, &Y, &M, &N, &K, &ntv, &mt, &ntl, &gm, &sched, &ws, &tcnt, &err};
-  return cudaLaunchKernel(tc_kernel(variant, act), dim3((unsigned)grid), dim3(kThreads), args, plan.smem, s);
+  // With split tiles the CTA that completes a tile waits for the others'
+  // parts: a cooperative launch keeps every CTA resident at once.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = sched.usk > 0 ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, tc_kernel(variant, act), args);
 }
 
 }  // namespace rocmfp4
