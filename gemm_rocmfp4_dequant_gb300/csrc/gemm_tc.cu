@@ -77,6 +77,7 @@ struct TcFmt {
   static constexpr int EBUF = V == 0 ? 2 : 1;            // epilogue buffers per output warp
 };
 constexpr uint32_t kEpiBytes = 16 * 32 * 4;  // one epilogue buffer: 16 tokens x 32 outputs, fp32
+constexpr uint32_t kFixStageBytes = (kThreads / 32) * 2 * kEpiBytes;  // split fix-up: two buffers per warp
 
 // Shared- and tensor-memory plan for a token-tile width nt (multiple of 16, <= 256).
 struct TcPlan {
@@ -191,49 +192,7 @@ struct Parts {
   RF4_DEV const float* slot(int k) const {
     return ws + (size_t)(2 * (bfirst + k) + (k == 0 && first_tail ? 1 : 0)) * kSlotFloats;
   }
-  // s = part 0 + part 1 + ... (in this order) for 16 tokens of one weight row;
-  // the loads of kBatch parts are in flight together.
-  static constexpr int kBatch = 2;
-  RF4_DEV void sum(int g, int row, float4 (&s)[4]) const {
-#pragma unroll 1
-    for (int k0 = 0; k0 < nparts; k0 += kBatch) {
-      float4 v[kBatch][4];
-#pragma unroll
-      for (int kk = 0; kk < kBatch; ++kk)
-        if (k0 + kk < nparts) {
-          const float* base = slot(k0 + kk);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v[kk][q] = __ldcg(reinterpret_cast<const float4*>(base + part_index(g, q, row)));
-        }
-#pragma unroll
-      for (int kk = 0; kk < kBatch; ++kk)
-        if (k0 + kk < nparts) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (k0 + kk == 0) {
-              s[q] = v[kk][q];
-            } else {
-              s[q].x += v[kk][q].x;
-              s[q].y += v[kk][q].y;
-              s[q].z += v[kk][q].z;
-              s[q].w += v[kk][q].w;
-            }
-          }
-        }
-    }
-  }
 };
-
-// Y[m + j][n] = tokens j = 0..15 of a summed split tile (s4[q] holds tokens
-// 4q .. 4q+3); a warp's lanes hold consecutive n, so each store is coalesced.
-RF4_DEV void store_fix16(const float4 (&s4)[4], float* Y, int M, int N, int m, int n) {
-  if (n >= N) return;
-  const float v[16] = {s4[0].x, s4[0].y, s4[0].z, s4[0].w, s4[1].x, s4[1].y, s4[1].z, s4[1].w,
-                       s4[2].x, s4[2].y, s4[2].z, s4[2].w, s4[3].x, s4[3].y, s4[3].z, s4[3].w};
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (m + j < M) Y[(size_t)(m + j) * N + n] = v[j];
-}
 
 // Waits (bounded: about two seconds of SM clock, acquire) until the written
 // half of a split-tile counter reaches `need`; false if it gave up.  The
@@ -440,9 +399,8 @@ struct Bars {
   uint64_t* empty;    // [stages] MMA commit
   uint64_t* rfull;    // [raw stages] TMA bytes
   uint64_t* rempty;   // [raw stages] one arrival per decode warp
-  uint64_t* cfull;    // chain finished (MMA commit)
-  uint64_t* cfree;    // slot C folded into R (output warps)
-  uint64_t* accfree;  // epilogue has read R and C (output warps)
+  uint64_t* cfull;    // [2] chain finished in accumulator slot 0 / 1 (MMA commit)
+  uint64_t* sfree;    // [2] accumulator slot consumed: folded or read out (output warps)
   uint64_t* fixbar;   // split fix-up: bulk copies of the parts (TMA bytes)
 };
 
@@ -521,9 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.rfull = b.empty + kMaxStages;
   b.rempty = b.rfull + F::RSTAGES;
   b.cfull = b.rempty + F::RSTAGES;
-  b.cfree = b.cfull + 1;
-  b.accfree = b.cfree + 1;
-  b.fixbar = b.accfree + 1;
+  b.sfree = b.cfull + 2;
+  b.fixbar = b.sfree + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 1);
   // Split tiles whose last arrival was this CTA's (at most two: a CTA's split
   // range has a part at each end), summed by all threads after the roles
@@ -544,9 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&b.rfull[i]), 1);
       mbar_init(smem_addr(&b.rempty[i]), kDecWarps);
     }
-    mbar_init(smem_addr(b.cfull), 1);
-    mbar_init(smem_addr(b.cfree), kOutThreads);
-    mbar_init(smem_addr(b.accfree), kOutThreads);
+    mbar_init(smem_addr(&b.cfull[0]), 1);
+    mbar_init(smem_addr(&b.cfull[1]), 1);
+    mbar_init(smem_addr(&b.sfree[0]), kOutThreads);
+    mbar_init(smem_addr(&b.sfree[1]), kOutThreads);
     mbar_init(smem_addr(b.fixbar), 1);
     fix[0] = 0;
     fence_mbar_init();
@@ -613,30 +571,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = instr_desc(ACT, nt);
       const uint64_t xdesc0 = smem_desc_sw128(smem_addr(stage0));
       const uint64_t adesc0 = smem_desc_sw128(smem_addr(stage0 + plan.xbytes));
-      const uint32_t slot_r = tmem, slot_c = tmem + plan.cstride;
       Ring r;
-      uint32_t n_cfree = 0, n_accfree = 0;
+      uint32_t uses0 = 0, uses1 = 0;  // chains written into each accumulator slot so far
       bool ok = true;
       ItemIter it(sched);
       Item w;
-      for (bool first = true; ok && it.next(sched, w); first = false) {
-        // both slots must have been read by the previous item's epilogue
-        if (!first && !mbar_wait_bounded(smem_addr(b.accfree), (n_accfree++) & 1u)) {
-          ok = false;
-          break;
-        }
+      for (int item = 0; ok && it.next(sched, w); ++item) {
         const int s0 = w.cb * F::SUBS, nsub = (w.ce - w.cb) * F::SUBS;
         const int nchains = (nsub + kSubsPerChain - 1) / kSubsPerChain;
+        const int base = item & 1;  // chain 0 of the item; later chains use the other slot
         int ks = s0;
         for (int c = 0; c < nchains && ok; ++c) {
           const int kend = s0 + (int)((int64_t)(c + 1) * nsub / nchains);
-          // chains 2.. reuse slot C once the output warps have folded it into R
-          if (c >= 2 && !mbar_wait_bounded(smem_addr(b.cfree), (n_cfree++) & 1u)) {
+          // a slot takes a new chain once the output warps have consumed its previous one
+          const int sl = c == 0 ? base : base ^ 1;
+          const uint32_t un = sl ? uses1 : uses0;
+          if (un > 0 && !mbar_wait_bounded(smem_addr(&b.sfree[sl]), (un - 1) & 1u)) {
             ok = false;
             break;
           }
+          if (sl) ++uses1; else ++uses0;
           tc_fence_after();
-          const uint32_t d = c == 0 ? slot_r : slot_c;
+          const uint32_t d = tmem + (uint32_t)sl * plan.cstride;
           for (int k0 = ks; ks < kend; ++ks, r.next(S)) {
             if (!mbar_wait_bounded(smem_addr(&b.full[r.stage]), r.phase)) {
               ok = false;
@@ -650,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_addr(&b.empty[r.stage]));
           }
           // The output warps act on every chain but the first of several.
-          if (ok && (c > 0 || nchains == 1)) mma_commit(smem_addr(b.cfull));
+          if (ok && (c > 0 || nchains == 1)) mma_commit(smem_addr(&b.cfull[sl]));
         }
       }
       if (!ok) atomicOr(err, kErrWaitTimeout);
@@ -685,18 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // tensor-memory lane = weight row of the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t slot_r = tmem + lane_off, slot_c = tmem + lane_off + plan.cstride;
     Emit<F::EBUF> out{smem + plan.off_epi + (uint32_t)quarter * F::EBUF * kEpiBytes, 0, quarter, lane, tma_y, &tmy, Y,
                       M, N};
-    uint32_t n_cfull = 0;
+    uint32_t n_cfull0 = 0, n_cfull1 = 0;  // chain completions awaited per slot
     bool ok = true;
     ItemIter it(sched);
     Item w;
-    while (ok && it.next(sched, w)) {
+    for (int item = 0; ok && it.next(sched, w); ++item) {
       int m0, n0;
       raster.tile(w.t, m0, n0);
       const int nsub = (w.ce - w.cb) * F::SUBS;
       const int nchains = (nsub + kSubsPerChain - 1) / kSubsPerChain;
+      // chain 0 accumulates in the item's base slot, later chains in the other
+      const int base = item & 1;
+      const uint32_t slot_b = tmem + lane_off + (uint32_t)base * plan.cstride;
+      const uint32_t slot_o = tmem + lane_off + (uint32_t)(base ^ 1) * plan.cstride;
       const bool whole = w.cb == 0 && w.ce == sched.nch;
       const int64_t t0 = (int64_t)(w.t - sched.dp_tiles) * sched.nch;  // first chunk of a split tile
       // A part of a split tile goes to the CTA's workspace slot 2b (the part
@@ -710,26 +669,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bfirst = whole ? 0 : sched.owner(t0);
       const int nparts = whole ? 1 : sched.owner(t0 + sched.nch - 1) - bfirst + 1;
       bool keep = false;
-      for (int c = nchains > 1 ? 1 : 0; c < nchains; ++c) {  // chain 0 of several stays in R
+      for (int c = nchains > 1 ? 1 : 0; c < nchains; ++c) {  // chain 0 of several stays in the base slot
         // the four output warps leave together, so their named barriers stay matched
-        if (!(ok = epi_all(warp_wait(smem_addr(b.cfull), (n_cfull++) & 1u)))) break;
+        const int sl = c == 0 ? base : base ^ 1;
+        const uint32_t nc = sl ? n_cfull1++ : n_cfull0++;
+        if (!(ok = epi_all(warp_wait(smem_addr(&b.cfull[sl]), nc & 1u)))) break;
         tc_fence_after();
-        if (c + 1 < nchains) {
-          // R += C, then C may take the next chain
+        if (nchains > 1) {
+          // base += other (fp32, round to nearest); the other slot is then
+          // free: for the next chain, or, after the last one, for the next
+          // item's chain 0 while this item's result is still being stored
 #pragma unroll 1
           for (int c0 = 0; c0 < nt; c0 += 16) {
             uint32_t a[16], v[16];
-            tmem_ld16(slot_r + (uint32_t)c0, a);
-            tmem_ld16(slot_c + (uint32_t)c0, v);
+            tmem_ld16(slot_b + (uint32_t)c0, a);
+            tmem_ld16(slot_o + (uint32_t)c0, v);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(v[j]));
-            tmem_st16(slot_r + (uint32_t)c0, a);
+            tmem_st16(slot_b + (uint32_t)c0, a);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
-          mbar_arrive(smem_addr(b.cfree));
-          continue;
+          mbar_arrive(smem_addr(&b.sfree[base ^ 1]));
+          if (c + 1 < nchains) continue;
         }
         if (!whole && final_item) {
           // Count first: if this arrival completes the tile, the part stays
@@ -747,25 +710,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             fix[2 + 5 * i] = m0;
             fix[3 + 5 * i] = n0;
             fix[4 + 5 * i] = (int)blockIdx.x - bfirst;
-            fix[5 + 5 * i] = nchains;
+            fix[5 + 5 * i] = base;
             fix[0] = i + 1;
           }
           if (keep) break;
         }
-        // last chain: R (+ C), 16 tokens at a time, to Y or to the workspace
+        // the base slot holds the item's sum: 16 tokens at a time to Y or to the workspace
 #pragma unroll 1
         for (int c0 = 0; c0 < nt; c0 += 16) {
-          uint32_t a[16], v[16];
-          tmem_ld16(slot_r + (uint32_t)c0, a);
-          if (nchains > 1) tmem_ld16(slot_c + (uint32_t)c0, v);
+          uint32_t a[16];
+          tmem_ld16(slot_b + (uint32_t)c0, a);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (nchains > 1) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(v[j]));
-          }
           if (c0 + 16 >= nt) {
             tc_fence_before();
-            mbar_arrive(smem_addr(b.accfree));  // both slots read: the next item may start
+            mbar_arrive(smem_addr(&b.sfree[base]));  // read out: the slot may take a new chain
           }
           if (whole) {
             out.store(a, m0 + c0, n0);
@@ -816,10 +774,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t fix_phase = 0;
   bool fix_ok = true;
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
+  // Every warp stages its 16 x 32 output blocks for tensor stores in two
+  // buffers of its own, just below the epilogue buffers.
+  Emit<2> fout{smem + plan.off_epi - kFixStageBytes + (uint32_t)warp * 2 * kEpiBytes, 0, warp & 3, lane, tma_y, &tmy,
+               Y, M, N};
 #pragma unroll 1
   for (int f = 0; f < nfix; ++f) {
     const int t = fix[1 + 5 * f], m0 = fix[2 + 5 * f], n0 = fix[3 + 5 * f];
-    const int own = fix[4 + 5 * f], nch_own = fix[5 + 5 * f];
+    const int own = fix[4 + 5 * f];
+    const uint32_t own_slot = tlane + (uint32_t)fix[5 + 5 * f] * plan.cstride;
     const Parts parts = tile_parts(sched, ws, t);
     const int ncopy = parts.nparts - (own >= 0 ? 1 : 0);
     if (threadIdx.x == 0) {
@@ -837,7 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int groups = nt / 16;
     constexpr uint32_t kGroupBytes = kTcRows * 16 * 4;  // one part, 16 tokens
     // token groups per window: every copied part's window fits in the rings
-    const int win = ncopy == 0 ? groups : min(groups, (int)(plan.off_epi / ((uint32_t)ncopy * kGroupBytes)));
+    // below the store staging buffers
+    const int win =
+        ncopy == 0 ? groups : min(groups, (int)((plan.off_epi - kFixStageBytes) / ((uint32_t)ncopy * kGroupBytes)));
     const bool from_ws = win == 0;  // too many parts for shared memory: read them in place
     const int step = from_ws ? 1 : win;
 #pragma unroll 1
@@ -867,14 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = pi % kTcRows, gl = pi / kTcRows, g = g0 + gl;
         float4 own4[4];
         if (own >= 0) {
-          uint32_t a[16], v[16];
-          tmem_ld16(tlane + (uint32_t)(16 * g), a);
-          if (nch_own > 1) tmem_ld16(tlane + plan.cstride + (uint32_t)(16 * g), v);
+          uint32_t a[16];
+          tmem_ld16(own_slot + (uint32_t)(16 * g), a);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (nch_own > 1) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(v[j]));
-          }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             own4[q] = make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
@@ -911,11 +871,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        store_fix16(s4, Y, M, N, m0 + 16 * g, n0 + row);
+        const uint32_t a[16] = {__float_as_uint(s4[0].x), __float_as_uint(s4[0].y), __float_as_uint(s4[0].z),
+                                __float_as_uint(s4[0].w), __float_as_uint(s4[1].x), __float_as_uint(s4[1].y),
+                                __float_as_uint(s4[1].z), __float_as_uint(s4[1].w), __float_as_uint(s4[2].x),
+                                __float_as_uint(s4[2].y), __float_as_uint(s4[2].z), __float_as_uint(s4[2].w),
+                                __float_as_uint(s4[3].x), __float_as_uint(s4[3].y), __float_as_uint(s4[3].z),
+                                __float_as_uint(s4[3].w)};
+        fout.store(a, m0 + 16 * g, n0);
       }
       __syncthreads();  // the window is consumed before the next copies overwrite it
     }
   }
+  if (lane == 0) bulk_wait_group_all();  // the fix-up's stores have completed
   if (!fix_ok) atomicOr(err, kErrWaitTimeout);
   tc_fence_before();
   __syncthreads();
