@@ -182,20 +182,17 @@ RF4_DEV void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kOutThreads) 
 // float4 access of one (g, q) covers 512 contiguous bytes.
 RF4_DEV size_t part_index(int g, int q, int row) { return (((size_t)g * 4 + q) * kTcRows + row) * 4; }
 
-// The parts of one split tile: part k is CTA (bfirst + k)'s, in its slot
-// 2 (bfirst + k), except that part 0 sits in slot 2 bfirst + 1 when it ends
-// that CTA's range instead of starting it.
+// The parts of one split tile: part k is CTA (bfirst + k)'s.  Part 0 stays
+// in CTA bfirst's tensor memory; part k >= 1 starts CTA (bfirst + k)'s range
+// and is in that CTA's workspace slot.
 struct Parts {
   const float* ws;
   int bfirst, nparts;
-  bool first_tail;
-  RF4_DEV const float* slot(int k) const {
-    return ws + (size_t)(2 * (bfirst + k) + (k == 0 && first_tail ? 1 : 0)) * kSlotFloats;
-  }
+  RF4_DEV const float* slot(int k) const { return ws + (size_t)(bfirst + k) * kSlotFloats; }
 };
 
-// Waits (bounded: about two seconds of SM clock, acquire) until the written
-// half of a split-tile counter reaches `need`; false if it gave up.  The
+// Waits (bounded: about two seconds of SM clock, acquire) until a split
+// tile's count of written parts reaches `need`; false if it gave up.  The
 // writers wait on nothing of the waiting CTA's, and a grid with split tiles
 // is launched cooperatively, so every writer is resident.
 RF4_DEV bool wait_parts_written(uint32_t* cnt, uint32_t need) {
@@ -203,7 +200,7 @@ RF4_DEV bool wait_parts_written(uint32_t* cnt, uint32_t need) {
   for (;;) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-    if ((v >> 16) >= need) return true;
+    if (v >= need) return true;
     if (clock64() - t0 > (1ll << 32)) return false;
     __nanosleep(32);
   }
@@ -215,7 +212,6 @@ RF4_DEV Parts tile_parts(const Sched& sc, const float* ws, int t) {
   p.ws = ws;
   p.bfirst = sc.owner(t0);
   p.nparts = sc.owner(t0 + sc.nch - 1) - p.bfirst + 1;
-  p.first_tail = sc.start(p.bfirst) != t0;
   return p;
 }
 
@@ -482,11 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.sfree = b.cfull + 2;
   b.fixbar = b.sfree + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 1);
-  // Split tiles whose last arrival was this CTA's (at most two: a CTA's split
-  // range has a part at each end), summed by all threads after the roles
-  // end: {count, then (tile, m0, n0, own part index or -1, own chains) per tile}.
+  // The split tile whose first part is this CTA's final item (at most one),
+  // summed by all threads after the roles end: {count, then (tile, m0, n0,
+  // own part index, own accumulator slot) per tile}.
   volatile int* fix = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* keep_flag = fix + 11;  // the output warps' count-first verdict
   volatile int* wait_flag = fix + 12;  // the fix-up's wait for written parts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -657,18 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t slot_b = tmem + lane_off + (uint32_t)base * plan.cstride;
       const uint32_t slot_o = tmem + lane_off + (uint32_t)(base ^ 1) * plan.cstride;
       const bool whole = w.cb == 0 && w.ce == sched.nch;
-      const int64_t t0 = (int64_t)(w.t - sched.dp_tiles) * sched.nch;  // first chunk of a split tile
-      // A part of a split tile goes to the CTA's workspace slot 2b (the part
-      // that starts its range) or 2b + 1 (the part that ends it).
-      float* part = whole ? nullptr
-                          : ws + (size_t)(2 * blockIdx.x + (t0 + w.cb == sched.start((int)blockIdx.x) ? 0 : 1)) *
-                                     kSlotFloats;
-      ItemIter peek = it;
-      Item nw;
-      const bool final_item = !peek.next(sched, nw);
-      const int bfirst = whole ? 0 : sched.owner(t0);
-      const int nparts = whole ? 1 : sched.owner(t0 + sched.nch - 1) - bfirst + 1;
-      bool keep = false;
+      // A split tile's first part (chunk 0 on) ends its CTA's range, so it is
+      // that CTA's final item: the CTA keeps it in tensor memory and sums
+      // the tile once its roles have ended.  Every other part starts its
+      // CTA's range and goes to that CTA's workspace slot.
+      const bool keep = !whole && w.cb == 0;
+      float* part = ws + (size_t)blockIdx.x * kSlotFloats;
       for (int c = nchains > 1 ? 1 : 0; c < nchains; ++c) {  // chain 0 of several stays in the base slot
         // the four output warps leave together, so their named barriers stay matched
         const int sl = c == 0 ? base : base ^ 1;
@@ -694,26 +683,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_addr(&b.sfree[base ^ 1]));
           if (c + 1 < nchains) continue;
         }
-        if (!whole && final_item) {
-          // Count first: if this arrival completes the tile, the part stays
-          // in tensor memory for the fix-up (low half of the counter:
-          // arrivals, high half: parts written).
+        if (keep) {
           if (row == 0) {
-            const uint32_t old = atomicAdd(&tcnt[w.t - sched.dp_tiles], 1u);
-            *keep_flag = (int)((old & 0xFFFFu) + 1u == (uint32_t)nparts);
-          }
-          epi_bar_sync();
-          keep = *keep_flag != 0;
-          if (keep && row == 0) {
             const int i = fix[0];
             fix[1 + 5 * i] = w.t;
             fix[2 + 5 * i] = m0;
             fix[3 + 5 * i] = n0;
-            fix[4 + 5 * i] = (int)blockIdx.x - bfirst;
+            fix[4 + 5 * i] = 0;  // this CTA's part is part 0
             fix[5 + 5 * i] = base;
             fix[0] = i + 1;
           }
-          if (keep) break;
+          break;
         }
         // the base slot holds the item's sum: 16 tokens at a time to Y or to the workspace
 #pragma unroll 1
@@ -737,24 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok || whole || keep) continue;
-      // Split tile, part written: publish it (and count the arrival too,
-      // unless the final item counted first).  The arrival that completes
-      // the tile records it; its CTA adds the parts in chunk order once its
-      // roles have ended, after waiting for every part to be written (each
-      // counted part is written by a CTA that waits on nothing meanwhile).
+      // Split tile, part written: count it for the tile's first CTA, which
+      // waits for the count after its own roles have ended.  A part is
+      // written before its CTA waits on anything of another CTA's, and the
+      // owners of later parts have higher indices, so no wait is circular.
       epi_bar_sync();  // every output thread's part stores precede the count
       if (row == 0) {
         __threadfence();  // this CTA's part is visible before the count
-        const uint32_t old = atomicAdd(&tcnt[w.t - sched.dp_tiles], final_item ? 0x10000u : 0x10001u);
-        if (!final_item && (old & 0xFFFFu) + 1u == (uint32_t)nparts) {
-          const int i = fix[0];
-          fix[1 + 5 * i] = w.t;
-          fix[2 + 5 * i] = m0;
-          fix[3 + 5 * i] = n0;
-          fix[4 + 5 * i] = -1;
-          fix[5 + 5 * i] = 0;
-          fix[0] = i + 1;
-        }
+        atomicAdd(&tcnt[w.t - sched.dp_tiles], 1u);
       }
     }
     if (lane == 0) bulk_wait_group_all();  // the stores have left shared memory and completed
@@ -911,7 +881,7 @@ int g_sms = 0;
 }  // namespace
 
 int tc_k_multiple(int variant) { return variant == 0 ? TcFmt<0>::KR : TcFmt<1>::KR; }
-size_t tc_ws_floats(int sms) { return 2 * (size_t)sms * kSlotFloats; }
+size_t tc_ws_floats(int sms) { return (size_t)sms * kSlotFloats; }
 size_t tc_cnt_words(int sms) { return 2 * (size_t)sms; }
 
 cudaError_t tc_prepare() {

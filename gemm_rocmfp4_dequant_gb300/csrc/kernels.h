@@ -55,7 +55,7 @@ struct TcArgs {
   uint32_t* err;
 };
 int tc_k_multiple(int variant);   // 256 (dual) or 512 (single-scale)
-size_t tc_ws_floats(int sms);     // 2 partial tiles of 128 x 256 fp32 per SM
+size_t tc_ws_floats(int sms);     // one partial tile of 128 x 256 fp32 per SM
 size_t tc_cnt_words(int sms);     // one counter per tile of the split region (at most 2 per SM)
 cudaError_t tc_prepare();         // resolves cuTensorMapEncodeTiled, sets the smem attributes
 cudaError_t launch_gemm_tc(int variant, int act, const TcArgs& a, cudaStream_t s);
