@@ -78,6 +78,7 @@ struct TcFmt {
 };
 constexpr uint32_t kEpiBytes = 16 * 32 * 4;  // one epilogue buffer: 16 tokens x 32 outputs, fp32
 constexpr uint32_t kFixStageBytes = (kThreads / 32) * 2 * kEpiBytes;  // split fix-up: two buffers per warp
+constexpr int kFixWinGroups = 2 * kThreads / 128;  // split fix-up: 16-token groups per window, at most
 
 // Shared- and tensor-memory plan for a token-tile width nt (multiple of 16, <= 256).
 struct TcPlan {
@@ -397,7 +398,7 @@ struct Bars {
   uint64_t* rempty;   // [raw stages] one arrival per decode warp
   uint64_t* cfull;    // [2] chain finished in accumulator slot 0 / 1 (MMA commit)
   uint64_t* sfree;    // [2] accumulator slot consumed: folded or read out (output warps)
-  uint64_t* fixbar;   // split fix-up: bulk copies of the parts (TMA bytes)
+  uint64_t* fixbar;   // [2] split fix-up: bulk copies of the parts into buffer 0 / 1 (TMA bytes)
 };
 
 // Slice S (two blocks, 64 K) of the raw chunk, for this thread's weight row,
@@ -477,10 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.cfull = b.rempty + F::RSTAGES;
   b.sfree = b.cfull + 2;
   b.fixbar = b.sfree + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b.fixbar + 2);
   // The split tile whose first part is this CTA's final item (at most one),
   // summed by all threads after the roles end: {count, then (tile, m0, n0,
-  // own part index, own accumulator slot) per tile}.
+  // own accumulator slot) per tile}.
   volatile int* fix = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* wait_flag = fix + 12;  // the fix-up's wait for written parts
 
@@ -500,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&b.cfull[1]), 1);
     mbar_init(smem_addr(&b.sfree[0]), kOutThreads);
     mbar_init(smem_addr(&b.sfree[1]), kOutThreads);
-    mbar_init(smem_addr(b.fixbar), 1);
+    mbar_init(smem_addr(&b.fixbar[0]), 1);
+    mbar_init(smem_addr(&b.fixbar[1]), 1);
     fix[0] = 0;
     fence_mbar_init();
   }
@@ -686,11 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (keep) {
           if (row == 0) {
             const int i = fix[0];
-            fix[1 + 5 * i] = w.t;
-            fix[2 + 5 * i] = m0;
-            fix[3 + 5 * i] = n0;
-            fix[4 + 5 * i] = 0;  // this CTA's part is part 0
-            fix[5 + 5 * i] = base;
+            fix[1 + 4 * i] = w.t;
+            fix[2 + 4 * i] = m0;
+            fix[3 + 4 * i] = n0;
+            fix[4 + 4 * i] = base;  // part 0 of the tile: this CTA's, in this slot
             fix[0] = i + 1;
           }
           break;
@@ -734,14 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   // ---- split fix-up: all threads; the stage and raw rings are free ----
-  // For each recorded tile: wait until every other part is written, bring
-  // those parts into shared memory by bulk copies (window by window), and
-  // add all parts in chunk order; this CTA's own part, when its final item
-  // counted first, is read from tensor memory (R + C, as it would have been
-  // written).  Tensor memory is released after the last fix-up.
+  // The recorded tile's part 0 is in this CTA's tensor memory.  Wait until
+  // the other parts are written, bring them into shared memory by bulk
+  // copies, window by window into two alternating buffers (the copies of
+  // the next window overlap the sums of this one), add the parts in chunk
+  // order and store the tile.  Tensor memory is released afterwards.
   tc_fence_after();
   const int nfix = fix[0];
-  uint32_t fix_phase = 0;
+  uint32_t fix_phase = 0;  // bit i: parity of fixbar[i]
   bool fix_ok = true;
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
   // Every warp stages its 16 x 32 output blocks for tensor stores in two
@@ -750,11 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                Y, M, N};
 #pragma unroll 1
   for (int f = 0; f < nfix; ++f) {
-    const int t = fix[1 + 5 * f], m0 = fix[2 + 5 * f], n0 = fix[3 + 5 * f];
-    const int own = fix[4 + 5 * f];
-    const uint32_t own_slot = tlane + (uint32_t)fix[5 + 5 * f] * plan.cstride;
+    const int t = fix[1 + 4 * f], m0 = fix[2 + 4 * f], n0 = fix[3 + 4 * f];
+    const uint32_t own_slot = tlane + (uint32_t)fix[4 + 4 * f] * plan.cstride;
     const Parts parts = tile_parts(sched, ws, t);
-    const int ncopy = parts.nparts - (own >= 0 ? 1 : 0);
+    const int ncopy = parts.nparts - 1;
     if (threadIdx.x == 0) {
       uint32_t* cnt = &tcnt[t - sched.dp_tiles];
       const bool okw = wait_parts_written(cnt, (uint32_t)ncopy);
@@ -769,76 +769,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int groups = nt / 16;
     constexpr uint32_t kGroupBytes = kTcRows * 16 * 4;  // one part, 16 tokens
-    // token groups per window: every copied part's window fits in the rings
-    // below the store staging buffers
-    const int win =
-        ncopy == 0 ? groups : min(groups, (int)((plan.off_epi - kFixStageBytes) / ((uint32_t)ncopy * kGroupBytes)));
+    // token groups per window: two windows of every copied part fit in the
+    // rings below the store staging buffers; at most kFixWinGroups, so that
+    // a thread holds at most two (row, group) pairs of a window
+    const uint32_t half_area = ((plan.off_epi - kFixStageBytes) / 2) & ~15u;
+    const int win = min(min(groups, kFixWinGroups), (int)(half_area / ((uint32_t)max(ncopy, 1) * kGroupBytes)));
     const bool from_ws = win == 0;  // too many parts for shared memory: read them in place
     const int step = from_ws ? 1 : win;
-#pragma unroll 1
-    for (int g0 = 0; g0 < groups; g0 += step) {
-      const int gw = min(step, groups - g0);
+    const int nwin = (groups + step - 1) / step;
+    // window w of the copied parts: part k (1..) at buffer (w & 1), slot k - 1
+    auto issue = [&](int w) {
+      const int g0 = w * step, gw = min(step, groups - g0);
       const uint32_t pbytes = (uint32_t)gw * kGroupBytes;
-      if (!from_ws && ncopy > 0) {
-        if (threadIdx.x == 0) {
-          // the rings' last generic-proxy accesses, and the parts acquired
-          // through the counter, come before the bulk copies
-          asm volatile("fence.proxy.async;" ::: "memory");
-          mbar_arrive_expect_tx(smem_addr(b.fixbar), pbytes * (uint32_t)ncopy);
-          for (int k = 0, sk = 0; k < parts.nparts; ++k) {
-            if (k == own) continue;
-            bulk_g2s(smem_addr(smem + (size_t)sk * pbytes), parts.slot(k) + (size_t)g0 * kTcRows * 16, pbytes,
-                     smem_addr(b.fixbar));
-            ++sk;
-          }
-        }
-        fix_ok = mbar_wait_bounded(smem_addr(b.fixbar), fix_phase) && fix_ok;
-        fix_phase ^= 1u;
+      uint8_t* buf = smem + (size_t)(w & 1) * half_area;
+      const uint32_t bar = smem_addr(&b.fixbar[w & 1]);
+      // the buffer's earlier generic-proxy accesses, and the parts acquired
+      // through the counter, come before the bulk copies
+      asm volatile("fence.proxy.async;" ::: "memory");
+      mbar_arrive_expect_tx(bar, pbytes * (uint32_t)ncopy);
+      for (int k = 1; k < parts.nparts; ++k)
+        bulk_g2s(smem_addr(buf + (size_t)(k - 1) * pbytes), parts.slot(k) + (size_t)g0 * kTcRows * 16, pbytes, bar);
+    };
+    if (!from_ws && threadIdx.x == 0) issue(0);
+#pragma unroll 1
+    for (int w = 0; w < nwin; ++w) {
+      const int g0 = w * step, gw = min(step, groups - g0);
+      const uint32_t pbytes = (uint32_t)gw * kGroupBytes;
+      const uint8_t* buf = smem + (size_t)(w & 1) * half_area;
+      if (!from_ws && threadIdx.x == 0 && w + 1 < nwin) issue(w + 1);
+      // part 0 of this thread's (row, group) pairs, from tensor memory, while
+      // the copies land: a warp's lanes are 32 rows of its tensor-memory lane
+      // quarter and share one group, as the tensor-memory loads need
+      uint32_t own[2][16];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int pi = threadIdx.x + i * kThreads;
+        if (pi < kTcRows * gw) tmem_ld16(own_slot + (uint32_t)(16 * (g0 + pi / kTcRows)), own[i]);
       }
-      // (row, group) pairs: a warp's lanes are 32 rows of its tensor-memory
-      // lane quarter and share one group, as the tensor-memory loads need
-#pragma unroll 1
-      for (int pi = threadIdx.x; pi < kTcRows * gw; pi += kThreads) {
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (!from_ws) {
+        fix_ok = mbar_wait_bounded(smem_addr(&b.fixbar[w & 1]), (fix_phase >> (w & 1)) & 1u) && fix_ok;
+        fix_phase ^= 1u << (w & 1);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int pi = threadIdx.x + i * kThreads;
+        if (pi >= kTcRows * gw) break;
         const int row = pi % kTcRows, gl = pi / kTcRows, g = g0 + gl;
-        float4 own4[4];
-        if (own >= 0) {
-          uint32_t a[16];
-          tmem_ld16(own_slot + (uint32_t)(16 * g), a);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            own4[q] = make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
-                                  __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3]));
-        }
         float4 s4[4];
-#pragma unroll 1
-        for (int k = 0, sk = 0; k < parts.nparts; ++k) {
-          float4 v4[4];
-          if (k == own) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v4[q] = own4[q];
-          } else if (from_ws) {
+        for (int q = 0; q < 4; ++q)
+          s4[q] = make_float4(__uint_as_float(own[i][4 * q]), __uint_as_float(own[i][4 * q + 1]),
+                              __uint_as_float(own[i][4 * q + 2]), __uint_as_float(own[i][4 * q + 3]));
+#pragma unroll 1
+        for (int k = 1; k < parts.nparts; ++k) {
+          float4 v4[4];
+          if (from_ws) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               v4[q] = __ldcg(reinterpret_cast<const float4*>(parts.slot(k) + part_index(g, q, row)));
-            ++sk;
           } else {
             const float4* src =
-                reinterpret_cast<const float4*>(smem + (size_t)sk * pbytes) + (size_t)gl * 4 * kTcRows + row;
+                reinterpret_cast<const float4*>(buf + (size_t)(k - 1) * pbytes) + (size_t)gl * 4 * kTcRows + row;
 #pragma unroll
             for (int q = 0; q < 4; ++q) v4[q] = src[q * kTcRows];
-            ++sk;
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            if (k == 0) {
-              s4[q] = v4[q];
-            } else {
-              s4[q].x += v4[q].x;
-              s4[q].y += v4[q].y;
-              s4[q].z += v4[q].z;
-              s4[q].w += v4[q].w;
-            }
+            s4[q].x += v4[q].x;
+            s4[q].y += v4[q].y;
+            s4[q].z += v4[q].z;
+            s4[q].w += v4[q].w;
           }
         }
         const uint32_t a[16] = {__float_as_uint(s4[0].x), __float_as_uint(s4[0].y), __float_as_uint(s4[0].z),
@@ -849,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __float_as_uint(s4[3].w)};
         fout.store(a, m0 + 16 * g, n0);
       }
-      __syncthreads();  // the window is consumed before the next copies overwrite it
+      __syncthreads();  // the window is consumed before copies overwrite its buffer
     }
   }
   if (lane == 0) bulk_wait_group_all();  // the fix-up's stores have completed
