@@ -26,8 +26,8 @@
  * Conventions shared by every entry point
  *   - Every pointer to matrix, activation or output data is DEVICE memory
  *     owned by the caller.  Calls do not allocate per call; a per-device
- *     workspace (split-reduction partials and counters: about 0.25 MiB per
- *     SM, 40 MiB on a 152-SM GPU) is allocated once, on first use, and
+ *     workspace (split-reduction partials and counters: about 0.18 MiB per
+ *     SM, 27 MiB on a 152-SM GPU) is allocated once, on first use, and
  *     released by rocmfp4_shutdown().
  *   - Calls on one device share that workspace: calls that overlap on the GPU
  *     (unordered streams, or graphs replayed concurrently) race and give wrong
