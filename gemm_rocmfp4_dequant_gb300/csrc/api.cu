@@ -105,6 +105,29 @@ rocmfp4_status check_shape(int64_t N, int64_t K, int variant) {
   return ROCMFP4_OK;
 }
 
+// Warps of a single-product streaming launch for `tiles` tiles of `nspans`
+// units of `unit_bytes` weight bytes, M activation rows, with room for `cap`
+// warps.  Units go to warps in contiguous equal ranges, four warps to a CTA.
+// When the tiles can be dealt out whole to CTAs that each stream at most
+// kAlignedCtaBytes of weights (and M <= 4), the grid has one CTA per run of
+// whole tiles: a tile is then split only between the warps of one CTA
+// (whenever the CTAs divide the tiles evenly), and the reduction never
+// takes its cross-CTA level, whose two L2 round trips at the end of the
+// launch cost more than the extra warps gain.  Otherwise (long rows, or
+// 8 activation rows) every warp that fits takes a share, which keeps more
+// bytes in flight.
+constexpr int64_t kAlignedCtaBytes = 40 * 4608;  // 40 dual units of 32 rows x 256 weights
+int64_t stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t M, int64_t cap) {
+  const int64_t units = tiles * nspans;
+  const int64_t maxc = cap / kStreamWarpsPerCta;
+  const int64_t tpc = (tiles + maxc - 1) / maxc;  // tiles per CTA
+  if (M <= 4 && tpc * nspans * unit_bytes <= kAlignedCtaBytes) {
+    const int64_t w = (tiles + tpc - 1) / tpc * kStreamWarpsPerCta;
+    return units < w ? units : w;
+  }
+  return units < cap ? units : cap;
+}
+
 rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K, int variant,
                        int act, cudaStream_t s) {
   rocmfp4_status st = check_shape(N, K, variant);
@@ -147,13 +170,14 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
     return ROCMFP4_OK;
   }
   const int64_t nspans = K / ku;
-  const int64_t units = (N + kStreamTileRows - 1) / kStreamTileRows * nspans;
+  const int64_t tiles = (N + kStreamTileRows - 1) / kStreamTileRows;
+  const int64_t units = tiles * nspans;
   for (int64_t m0 = 0; m0 < M; m0 += 8) {
     const int mc = (int)(M - m0 < 8 ? M - m0 : 8);
     const int mb = stream_mb_for(mc);
     const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
     const int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
-    const int64_t wact = units < cap ? units : cap;
+    const int64_t wact = stream_warps(tiles, nspans, ku * block_bytes_of(variant), mc, cap);
     const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
     GemvArgs a{};
     a.W = static_cast<const uint8_t*>(W);
@@ -236,20 +260,21 @@ rocmfp4_status chain(const rocmfp4_gemv_op* ops, int count, int64_t M, int varia
       ++i;
       continue;
     }
-    // a run of eligible products, at most kChainOps
+    // a run of eligible products, at most kChainOps; each product's units go
+    // to the warps a single call would give them, so the sums are the same
     int n = 0;
-    int64_t umax = 0;
+    int64_t wmax = 0;
+    GemvArgs args[kChainOps];
     while (i + n < count && n < kChainOps && ops[i + n].N > 0 && chain_eligible(ops[i + n], M, variant)) {
+      const rocmfp4_gemv_op& op = ops[i + n];
       const int64_t ku = stream_weights_per_unit(variant);
-      const int64_t u = (ops[i + n].N + kStreamTileRows - 1) / kStreamTileRows * (ops[i + n].K / ku);
-      umax = u > umax ? u : umax;
+      const int64_t w =
+          stream_warps((op.N + kStreamTileRows - 1) / kStreamTileRows, op.K / ku, ku * block_bytes_of(variant), M, cap);
+      args[n] = stream_args(d, op.W, op.X, op.Y, M, op.N, op.K, variant, w);
+      wmax = w > wmax ? w : wmax;
       ++n;
     }
-    const int64_t wact = umax < cap ? umax : cap;
-    const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
-    GemvArgs args[kChainOps];
-    for (int g = 0; g < n; ++g)
-      args[g] = stream_args(d, ops[i + g].W, ops[i + g].X, ops[i + g].Y, M, ops[i + g].N, ops[i + g].K, variant, wact);
+    const int ctas = (int)((wmax + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
     cudaError_t e = n == 1 ? launch_gemv_stream(variant, act, args[0], ctas, s)
                            : launch_gemv_chain(variant, act, args, n, d->gbar, ctas, s);
     if (e != cudaSuccess) return cuda_fail(e, n == 1 ? "streaming kernel launch" : "chained streaming launch");
@@ -280,7 +305,8 @@ rocmfp4_status gate_up(const void* W, const void* X, float* Y, int64_t M, int64_
   if ((st = device_state(&d)) != ROCMFP4_OK) return st;
   const int64_t ku = stream_weights_per_unit(variant);
   const int64_t nspans = K / ku;
-  const int64_t units = (I + kStreamTileRows / 2 - 1) / (kStreamTileRows / 2) * nspans;
+  const int64_t tiles = (I + kStreamTileRows / 2 - 1) / (kStreamTileRows / 2);  // 16 gate and 16 up rows each
+  const int64_t units = tiles * nspans;
   if (K % ku != 0 || !aligned16(W) || !aligned16(X) || units >= (int64_t(1) << 31))
     return fail(ROCMFP4_ERR_UNSUPPORTED,
                 "gate/up product: K must be a multiple of 256 (dual) or 512 (single-scale), W and X 16-byte aligned");
@@ -297,7 +323,7 @@ rocmfp4_status gate_up(const void* W, const void* X, float* Y, int64_t M, int64_
   a.M = (int)M;
   a.nspans = nspans;
   a.units = units;
-  a.wact = units < cap ? units : cap;
+  a.wact = stream_warps(tiles, nspans, ku * block_bytes_of(variant), M, cap);
   a.ws = d->ws;
   a.cnt = d->cnt;
   a.err = d->err;
