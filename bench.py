@@ -45,13 +45,16 @@ sys.path.insert(0, ROOT)
 
 LAYER = [("qkv", 7168, 5120), ("o", 5120, 6144), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
 LM_HEAD = ("lm_head", 152064, 5120)
+ROLES = ("qkv", "o", "gate_up", "down", "lm_head")
 N_LAYERS = 64
 PREFILL_M = (512, 4096, 23552)
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "ROCmFP4 GEMV weight GB/s (% of HBM peak); W4A16 GEMM TFLOP/s (% peak)"
 DATA = "synthetic (seeded SplitMix64 weight bytes, Box-Muller N(0,1) activations)"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_stream_layer_dual_m1.md")
-GEMV_SOURCE = os.path.join(ROOT, "gemm_rocmfp4_dequant_gb300", "csrc", "gemv.cu")
+# the kernel and the host code that sizes its grid: the traffic record holds while both are unchanged
+GEMV_SOURCES = (os.path.join(ROOT, "gemm_rocmfp4_dequant_gb300", "csrc", "gemv.cu"),
+                os.path.join(ROOT, "gemm_rocmfp4_dequant_gb300", "csrc", "api.cu"))
 
 
 def peaks():
@@ -85,11 +88,12 @@ def weight_bytes(mats, variant=0):
 
 def gemv_traffic():
     """DRAM bytes per launch of the streaming GEMV on the layer shapes, from the
-    committed ncu summary, if that capture was taken on the current kernel source
-    (its sha256 is recorded in the summary); else None."""
+    committed ncu summary, if that capture was taken on the current kernel and
+    launch-sizing source (the sha256 of both files is recorded in the summary);
+    else None."""
     try:
         text = open(TRAFFIC_FILE).read()
-        src = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+        src = hashlib.sha256(b"".join(open(f, "rb").read() for f in GEMV_SOURCES)).hexdigest()
     except OSError:
         return None
     m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
@@ -777,21 +781,41 @@ def run_single(args, world):
 
 # ---- whole-model decode step (config: 64 layers x 4 matrices + LM head) --------------------------
 
-class ModelStep:
-    """All weights resident (12.5 GB dual); one CUDA graph of 257 GEMV launches per
-    token, each with its own activation vector (outputs are not chained)."""
+def parse_layouts(text):
+    """Block layout per tensor role, "role=dual|fast,..." over the roles qkv, o,
+    gate_up, down, lm_head; roles not named are dual."""
+    out = {r: 0 for r in ROLES}
+    for item in filter(None, (text or "").split(",")):
+        role, _, v = item.partition("=")
+        if role not in out or v not in ("dual", "fast"):
+            raise SystemExit(f"--layouts: bad item {item!r} (roles {', '.join(ROLES)}; layouts dual, fast)")
+        out[role] = 0 if v == "dual" else 1
+    return out
 
-    def __init__(self, variant=0):
+
+def role_of(name):
+    return name.split(".")[-1]
+
+
+class ModelStep:
+    """All weights resident (12.5 GB all dual); one CUDA graph of 257 GEMV launches
+    per token, each with its own activation vector (outputs are not chained).
+    Each matrix takes the block layout that `layouts` gives its tensor role."""
+
+    def __init__(self, layouts=None):
         import torch
 
         import gemm_rocmfp4_dequant_gb300 as rf4
         import synth
         import synth.device
-        self.rf4, self.variant = rf4, variant
+        self.rf4 = rf4
+        self.layouts = layouts or {r: 0 for r in ROLES}
         self.mats = [(f"l{l}.{n}", N, K) for l in range(N_LAYERS) for (n, N, K) in LAYER] + [LM_HEAD]
+        self.variants = [self.layouts[role_of(n)] for n, _, _ in self.mats]
         self.W, self.X, self.Y = [], [], []
         for i, (name, N, K) in enumerate(self.mats):
             layer, m = (i // 4, i % 4) if i < 4 * N_LAYERS else (N_LAYERS, 4)
+            variant = self.variants[i]
             w = torch.empty(N * rf4.row_bytes(K, variant), dtype=torch.uint8, device="cuda")
             synth.device.fill_weights(w, N, K, variant, seed=0, stream=synth.weight_stream(layer, m))
             x = torch.empty((1, K), dtype=torch.int16, device="cuda")
@@ -812,20 +836,20 @@ class ModelStep:
         torch.cuda.synchronize()
 
     def run(self):
-        for (name, N, K), w, x, y in zip(self.mats, self.W, self.X, self.Y):
-            self.rf4.gemm(w, x, N, K, self.variant, Y=y)
+        for (name, N, K), v, w, x, y in zip(self.mats, self.variants, self.W, self.X, self.Y):
+            self.rf4.gemm(w, x, N, K, v, Y=y)
 
 
 def run_model(args, world):
     import torch
-    S = ModelStep()
+    S = ModelStep(parse_layouts(args.layouts))
     with ClockSampler(torch.cuda.current_device()) as clk:
         t = time_steps(lambda i: S.graph.replay(), args.steps, args.warmup, world)
     t = max_over_ranks(t, world)
-    sb = step_bytes(S.mats)
+    sb = sum(step_bytes([m], v) for m, v in zip(S.mats, S.variants))
     res = dict(value=world * sb * args.steps / t / 1e9, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
                tok_s=world * args.steps / t, gpu_launches=len(S.mats) * args.steps, step_bytes=sb,
-               weight_gb=round(weight_bytes(S.mats) / 1e9, 3))
+               weight_gb=round(sum(weight_bytes([m], v) for m, v in zip(S.mats, S.variants)) / 1e9, 3))
     del S
     torch.cuda.empty_cache()
     return res
@@ -895,6 +919,8 @@ def main():
     ap.add_argument("--workload", default="layer",
                     choices=["layer", "single", "sweep", "model", "prefill", "gate_up", "attention", "quantize"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layouts", default="", help="model workload: block layout per tensor role, "
+                    "e.g. qkv=dual,o=dual,gate_up=fast,down=fast,lm_head=dual (default: all dual)")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill object out of the layer line")
     ap.add_argument("--prefill-m", type=str, default=",".join(str(m) for m in PREFILL_M),
                     help="comma-separated token counts of the prefill GEMM")
@@ -925,6 +951,10 @@ def main():
                      "l2": "two resident 356 MB sources, larger than L2"},
     }
     cfg = cfgs[args.workload]
+    if args.workload == "model" and args.layouts:
+        lay = parse_layouts(args.layouts)
+        names = ",".join(f"{r}={'dual' if v == 0 else 'fast'}" for r, v in lay.items())
+        cfg = dict(cfg, workload=cfg["workload"].replace(", dual,", f", layouts {names},"), variant="per role")
 
     if args.impl == "reference":
         if rank == 0:

@@ -25,7 +25,7 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_quantize", "rocmfp4_gemv_chain", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_quantize", "rocmfp4_gemv_chain", "rocmfp4_gemv_chain_mixed", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
@@ -65,6 +65,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                      c_int),
         "rocmfp4_quantize": ([vp, c_int, vp, i64, i64, c_int, vp], c_int),
         "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
+        "rocmfp4_gemv_chain_mixed": ([ctypes.POINTER(GemvOp), ctypes.POINTER(c_int), c_int, i64, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
         "rocmfp4_device_error_bits": ([vp], u32),
@@ -205,24 +206,34 @@ def decode_attention(q, K, V, lens, Hkv: int, Tmax: int, scale: float, variant: 
     return out
 
 
-def gemv_chain(ops, variant: int = DUAL, stream=None):
+def gemv_chain(ops, variant=DUAL, stream=None):
     """Runs products in order, as gemm() for each: ops is a list of (W, X, Y, N, K)
-    with X [M, K] (all float16 or all bfloat16, one M) and Y [M, N] float32."""
+    with X [M, K] (all float16 or all bfloat16, one M) and Y [M, N] float32.
+    variant is one block layout for every product, or a sequence with one per
+    product (rocmfp4_gemv_chain_mixed)."""
     torch = _torch()
     if not ops:
         return
+    mixed = not isinstance(variant, int)
+    variants = [int(v) for v in variant] if mixed else [variant] * len(ops)
+    if len(variants) != len(ops):
+        raise ValueError("one variant per product")
     M = ops[0][1].shape[0] if ops[0][1].dim() == 2 else 1
     act = _act_of(ops[0][1])
     arr = (GemvOp * len(ops))()
     for i, (W, X, Y, N, K) in enumerate(ops):
-        _check_w(W, N, K, variant)
+        _check_w(W, N, K, variants[i])
         Xm = X.view(1, -1) if X.dim() == 1 else X
         if not Xm.is_cuda or not Xm.is_contiguous() or tuple(Xm.shape) != (M, K) or _act_of(Xm) != act:
             raise ValueError(f"product {i}: X must be a contiguous [M, K] CUDA tensor of the chain's dtype")
         if Y.dtype != torch.float32 or not Y.is_contiguous() or Y.numel() < M * N:
             raise ValueError(f"product {i}: Y must be a contiguous float32 tensor with M*N elements")
         arr[i] = GemvOp(W.data_ptr(), Xm.data_ptr(), Y.data_ptr(), N, K)
-    _check(load().rocmfp4_gemv_chain(arr, len(ops), M, variant, act, _stream(stream)), "rocmfp4_gemv_chain")
+    if mixed:
+        varr = (ctypes.c_int * len(ops))(*variants)
+        _check(load().rocmfp4_gemv_chain_mixed(arr, varr, len(ops), M, act, _stream(stream)), "rocmfp4_gemv_chain_mixed")
+    else:
+        _check(load().rocmfp4_gemv_chain(arr, len(ops), M, variant, act, _stream(stream)), "rocmfp4_gemv_chain")
 
 
 def quantize(src, variant: int = DUAL, W=None, stream=None):

@@ -426,6 +426,34 @@ rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op* ops, int count, int64_t
   return chain(ops, count, M, variant, act, reinterpret_cast<cudaStream_t>(stream));
 }
 
+rocmfp4_status rocmfp4_gemv_chain_mixed(const rocmfp4_gemv_op* ops, const rocmfp4_variant* variants, int count,
+                                        int64_t M, rocmfp4_act act, rocmfp4_stream_t stream) {
+  if (count < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative count");
+  if (count == 0) return ROCMFP4_OK;
+  if (ops == nullptr || variants == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "ops or variants is NULL");
+  if (!valid_act(act)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown activation type");
+  if (M < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  // every product is checked before any launch, as in a single-layout chain
+  for (int i = 0; i < count; ++i) {
+    const rocmfp4_gemv_op& op = ops[i];
+    rocmfp4_status st = check_shape(op.N, op.K, variants[i]);
+    if (st != ROCMFP4_OK) return fail(st, "product " + std::to_string(i) + ": " + t_last_error);
+    if (M == 0 || op.N == 0) continue;
+    if (op.Y == nullptr || (op.K > 0 && (op.W == nullptr || op.X == nullptr)))
+      return fail(ROCMFP4_ERR_INVALID_ARG, "product " + std::to_string(i) + ": NULL pointer");
+  }
+  // runs of products with one layout, each a single-layout chain, in order
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int i = 0; i < count;) {
+    int n = 1;
+    while (i + n < count && variants[i + n] == variants[i]) ++n;
+    rocmfp4_status st = chain(ops + i, n, M, variants[i], act, s);
+    if (st != ROCMFP4_OK) return st;
+    i += n;
+  }
+  return ROCMFP4_OK;
+}
+
 rocmfp4_status rocmfp4_dequant(const void* W, void* out, rocmfp4_out_dtype out_dtype, int64_t N, int64_t K,
                                rocmfp4_variant variant, rocmfp4_stream_t stream) {
   rocmfp4_status st = check_shape(N, K, variant);

@@ -194,6 +194,23 @@ typedef struct rocmfp4_gemv_op {
 rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op *ops, int count, int64_t M,
                                   rocmfp4_variant variant, rocmfp4_act act, rocmfp4_stream_t stream);
 
+/* rocmfp4_gemv_chain over products whose weights have different block
+ * layouts: product i's W is in layout variants[i].
+ *
+ * ("Tensor-Aware Presets": a model quantised with a preset mixes the 18- and
+ * 17-byte layouts across tensor roles, so the engine picks the layout per
+ * tensor.  The pages name six presets but list none of their contents: the
+ * caller maps its tensors to layouts.)
+ *   - variants is host memory of `count` entries, read during the call.
+ *   - The result is that of calling rocmfp4_gemm_ex for each product in turn
+ *     with its own layout, bit for bit.  Consecutive products of one layout
+ *     run as one single-layout chain; a change of layout starts another.
+ *   - Every product is checked (shape, layout, pointers) before any launch;
+ *     otherwise arguments, aliasing rules and errors as rocmfp4_gemv_chain. */
+rocmfp4_status rocmfp4_gemv_chain_mixed(const rocmfp4_gemv_op *ops, const rocmfp4_variant *variants,
+                                        int count, int64_t M, rocmfp4_act act,
+                                        rocmfp4_stream_t stream);
+
 /* Y = X . W^T for M <= 8 without allocating device memory.
  *
  * For callers that cannot call cudaMalloc where they run the product: an

@@ -21,6 +21,20 @@ def test_layer_and_model_bytes():
     assert bench.matrix_bytes(7168, 5120, variant=1) == 7168 * 160 * 17
 
 
+def test_layout_map_per_tensor_role():
+    lay = bench.parse_layouts("gate_up=fast,down=fast")
+    assert lay == {"qkv": 0, "o": 0, "gate_up": 1, "down": 1, "lm_head": 0}
+    assert bench.parse_layouts("") == {r: 0 for r in bench.ROLES}
+    for bad in ("ffn=fast", "qkv=fp8", "qkv"):
+        with pytest.raises(SystemExit):
+            bench.parse_layouts(bad)
+    assert bench.role_of("l12.gate_up") == "gate_up" and bench.role_of("lm_head") == "lm_head"
+    # mixed step bytes: each matrix at its own block size
+    mats = [("l0.qkv", 7168, 5120), ("l0.gate_up", 34816, 5120)]
+    got = sum(bench.step_bytes([m], lay[bench.role_of(m[0])]) for m in mats)
+    assert got == 7168 * 160 * 18 + 34816 * 160 * 17 + 2 * 5120 * 2 + 4 * (7168 + 34816)
+
+
 def test_gate_up_bytes():
     # the fused product reads the 2I x K matrix of the layer's gate+up, one x, writes I outputs
     I, K = bench.GATE_UP
@@ -42,12 +56,17 @@ def test_quantize_bytes():
 def test_traffic_record_needs_the_measured_source(tmp_path, monkeypatch):
     src = tmp_path / "gemv.cu"
     src.write_text("kernel v1\n")
+    host = tmp_path / "api.cu"
+    host.write_text("grid v1\n")
     rec = tmp_path / "rec.md"
-    sha = hashlib.sha256(b"kernel v1\n").hexdigest()
+    sha = hashlib.sha256(b"kernel v1\ngrid v1\n").hexdigest()
     rec.write_text(f"notes\nsource_sha256: {sha}\ndram_bytes_per_launch: qkv=10, o=20, gate_up=30, down=40\n")
-    monkeypatch.setattr(bench, "GEMV_SOURCE", str(src))
+    monkeypatch.setattr(bench, "GEMV_SOURCES", (str(src), str(host)))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
     assert bench.gemv_traffic() == {"qkv": 10, "o": 20, "gate_up": 30, "down": 40}
+    host.write_text("grid v2\n")  # launch sizing changed since the capture: no traffic figure
+    assert bench.gemv_traffic() is None
+    host.write_text("grid v1\n")
     src.write_text("kernel v2\n")  # kernel changed since the capture: no traffic figure
     assert bench.gemv_traffic() is None
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.md"))
