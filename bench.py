@@ -461,23 +461,28 @@ def per_matrix_kernel_times(L: GemvStep, reps=None):
 
 
 def e2e_rate(L: GemvStep, steps, warmup, world):
-    """The metric through the public API with host buffers: every step copies each
-    matrix's activations from pinned host memory, runs the products and reads every
-    output back into pinned host memory; weights stay resident."""
+    """The metric through the public API with host buffers: every step copies the
+    step's activations (all matrices', packed in one pinned host buffer) to the
+    device, runs the products through the API and reads all outputs back into one
+    pinned host buffer; weights stay resident."""
     import torch
-    hx = [[x.cpu().pin_memory() for x in Xc] for Xc in L.X]
-    hy = [[torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in Yc] for Yc in L.Y]
-    dx = [torch.empty_like(x) for x in L.X[0]]
-    dy = [torch.empty_like(y) for y in L.Y[0]]
-    h2d = sum(x.numel() * x.element_size() for x in dx)
-    d2h = sum(y.numel() * 4 for y in dy)
+    xs = [x.numel() for x in L.X[0]]
+    ys = [y.numel() for y in L.Y[0]]
+    hx = [torch.cat([x.reshape(-1) for x in Xc]).cpu().pin_memory() for Xc in L.X]
+    hy = [torch.empty(sum(ys), dtype=torch.float32).pin_memory() for _ in L.Y]
+    dx_all = torch.empty(sum(xs), dtype=L.X[0][0].dtype, device="cuda")
+    dy_all = torch.empty(sum(ys), dtype=torch.float32, device="cuda")
+    dx = [v.view(x.shape) for v, x in zip(torch.split(dx_all, xs), L.X[0])]
+    dy = [v.view(y.shape) for v, y in zip(torch.split(dy_all, ys), L.Y[0])]
+    h2d = dx_all.numel() * dx_all.element_size()
+    d2h = dy_all.numel() * 4
 
     def one(i):
         r = i % L.copies
+        dx_all.copy_(hx[r], non_blocking=True)
         for m, (name, N, K) in enumerate(L.mats):
-            dx[m].copy_(hx[r][m], non_blocking=True)
             L.rf4.gemm(L.W[r][m], dx[m], N, K, L.variant, Y=dy[m])
-            hy[r][m].copy_(dy[m], non_blocking=True)
+        hy[r].copy_(dy_all, non_blocking=True)
 
     t = time_steps(one, steps, warmup, world)
     return t, h2d, d2h
