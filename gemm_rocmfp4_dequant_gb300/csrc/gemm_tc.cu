@@ -24,11 +24,19 @@
 // Accumulation chains.  The tensor core adds each 16-deep partial product
 // into its fp32 accumulator with a rounding whose error grows with the chain
 // length (at K = 17408 one chain leaves a relative L2 error near 1.2e-5).
-// K is therefore cut into chains of at most kChainK: chain 0 accumulates in
-// tensor-memory slot R, every later chain in slot C; after each later chain
-// the output warps add C into R (fp32, round to nearest), and the epilogue
-// stores R + C.  The order of all additions is fixed, so results are
-// deterministic.
+// K is therefore cut into chains of at most kChainK: chain 0 of a tile
+// accumulates in one of the two tensor-memory slots (its base slot), every
+// later chain in the other; after each later chain the output warps add the
+// other slot into the base slot (fp32, round to nearest).  The base slot
+// alternates between consecutive tiles, so the next tile's chain 0 runs in
+// the freed slot while the finished tile is still being stored.  The order
+// of all additions is fixed, so results are deterministic.
+//
+// Split tiles (the last wave and a half when the tile count is not a
+// multiple of the SM count) are cut by K across consecutive CTAs.  The CTA
+// holding a tile's first chunk keeps that part in tensor memory and, after
+// its roles end, adds the other parts (written to a workspace) in chunk
+// order; such a launch is cooperative because that CTA waits for the others.
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer of the X slices
