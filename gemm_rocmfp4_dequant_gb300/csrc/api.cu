@@ -193,6 +193,8 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
     a.ws = d->ws;
     a.cnt = d->cnt;
     a.err = d->err;
+    // A grid of at most two CTAs per SM takes the deeper rings (M <= 2).
+    a.deep = mb <= 2 && ctas <= 2 * d->sms ? 1 : 0;
     cudaError_t e = launch_gemv_stream(variant, act, a, ctas, s);
     if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
     g_launches.fetch_add(1);

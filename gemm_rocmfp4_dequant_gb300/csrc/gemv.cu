@@ -64,16 +64,19 @@ constexpr int stage_bytes() { return kTileRows * Fmt<V>::SPAN + MB * Fmt<V>::KU 
 
 // Stages per warp: as many as fit in about 54 KB per CTA (four CTAs, 16 warps
 // per SM), at least 2 (one unit in flight while the previous one computes).
-template <int V, int MB>
+// DEEP = 1: about 108 KB per CTA (two CTAs per SM), for grids that place at
+// most two CTAs on an SM: more of a small matrix is in flight, and more of it
+// streams before the preceding grid ends.
+template <int V, int MB, int DEEP = 0>
 constexpr int stages() {
-  constexpr int n = (54 * 1024) / (kWarps * stage_bytes<V, MB>());
+  constexpr int n = ((DEEP ? 108 : 54) * 1024) / (kWarps * stage_bytes<V, MB>());
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-template <int V, int MB>
+template <int V, int MB, int DEEP = 0>
 constexpr size_t smem_bytes() {
-  return (size_t)kWarps * stages<V, MB>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB>() * 8 + 16 +
-         cta_red_bytes<MB>();
+  return (size_t)kWarps * stages<V, MB, DEEP>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB, DEEP>() * 8 +
+         16 + cta_red_bytes<MB>();
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -678,10 +681,10 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
 // product g > 0 of a chain, all warps' work on product g - 1 (grid barrier).
 // The barrier also makes the split-tile workspace free for the next product.
 // EPI = 1: the gate/up mode (single-product launches only).
-template <int V, int ACT, int MB, int NOPS, int EPI>
+template <int V, int ACT, int MB, int NOPS, int EPI, int DEEP>
 __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
   using F = Fmt<V>;
-  constexpr int NS = stages<V, MB>();
+  constexpr int NS = stages<V, MB, DEEP>();
   constexpr int SB = stage_bytes<V, MB>();
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -825,11 +828,18 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
 template <int V, int ACT, int NOPS, int EPI>
 const void* kernel_for_mb(int mb) {
   switch (mb) {
-    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS, EPI>);
-    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS, EPI>);
-    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS, EPI>);
-    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS, EPI>);
+    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS, EPI, 0>);
+    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS, EPI, 0>);
+    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS, EPI, 0>);
+    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS, EPI, 0>);
   }
+}
+
+// The deep-ring instance of a single plain product (MB = 1 or 2 only).
+template <int V, int ACT>
+const void* deep_kernel_for_mb(int mb) {
+  return mb == 1 ? reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, 1, 0, 1>)
+                 : reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, 1, 0, 1>);
 }
 
 template <int EPI>
@@ -838,8 +848,13 @@ const void* single_kernel(int variant, int act, int mb) {
   return act == 0 ? kernel_for_mb<1, 0, 1, EPI>(mb) : kernel_for_mb<1, 1, 1, EPI>(mb);
 }
 
-// kind 0: single product, 1: chain, 2: single gate/up product.
+// kind 0: single product, 1: chain, 2: single gate/up product, 3: single
+// product with the deep ring (MB <= 2).
 const void* stream_kernel(int variant, int act, int mb, int kind) {
+  if (kind == 3) {
+    if (variant == 0) return act == 0 ? deep_kernel_for_mb<0, 0>(mb) : deep_kernel_for_mb<0, 1>(mb);
+    return act == 0 ? deep_kernel_for_mb<1, 0>(mb) : deep_kernel_for_mb<1, 1>(mb);
+  }
   if (kind == 1) {
     if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, kChainOps, 0>(mb) : kernel_for_mb<0, 1, kChainOps, 0>(mb);
     return act == 0 ? kernel_for_mb<1, 0, kChainOps, 0>(mb) : kernel_for_mb<1, 1, kChainOps, 0>(mb);
@@ -848,10 +863,10 @@ const void* stream_kernel(int variant, int act, int mb, int kind) {
 }
 
 template <int V>
-size_t smem_for_mb(int mb) {
+size_t smem_for_mb(int mb, int deep) {
   switch (mb) {
-    case 1: return smem_bytes<V, 1>();
-    case 2: return smem_bytes<V, 2>();
+    case 1: return deep ? smem_bytes<V, 1, 1>() : smem_bytes<V, 1>();
+    case 2: return deep ? smem_bytes<V, 2, 1>() : smem_bytes<V, 2>();
     case 4: return smem_bytes<V, 4>();
     default: return smem_bytes<V, 8>();
   }
@@ -863,12 +878,16 @@ int stream_mb_for(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 int stream_weights_per_unit(int variant) { return variant == 0 ? Fmt<0>::KU : Fmt<1>::KU; }
 
-size_t stream_smem_bytes(int variant, int mb) { return variant == 0 ? smem_for_mb<0>(mb) : smem_for_mb<1>(mb); }
+size_t stream_smem_bytes(int variant, int mb, int deep) {
+  return variant == 0 ? smem_for_mb<0>(mb, deep) : smem_for_mb<1>(mb, deep);
+}
 
 cudaError_t stream_prepare(int variant, int act, int mb) {
-  for (int kind = 0; kind < 3; ++kind) {
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel(variant, act, mb, kind),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes(variant, mb));
+  for (int kind = 0; kind < 4; ++kind) {
+    if (kind == 3 && mb > 2) break;
+    cudaError_t e =
+        cudaFuncSetAttribute(stream_kernel(variant, act, mb, kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem_bytes(variant, mb, kind == 3 ? 1 : 0));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -878,10 +897,10 @@ cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm) {
   // The chain instance must fit as many CTAs per SM (all of its CTAs are co-resident).
   int one = 0, chain = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&one, stream_kernel(variant, act, mb, 0), kWarps * 32,
-                                                                stream_smem_bytes(variant, mb));
+                                                                stream_smem_bytes(variant, mb, 0));
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&chain, stream_kernel(variant, act, mb, 1), kWarps * 32,
-                                                    stream_smem_bytes(variant, mb));
+                                                    stream_smem_bytes(variant, mb, 0));
   if (e != cudaSuccess) return e;
   *ctas_per_sm = one < chain ? one : chain;
   return cudaSuccess;
@@ -967,7 +986,8 @@ cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb);
+  const int deep = a.deep && !a.epi && mb <= 2 ? 1 : 0;
+  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb, deep);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -975,7 +995,7 @@ cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, a.epi ? 2 : 0), args);
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, a.epi ? 2 : (deep ? 3 : 0)), args);
 }
 
 cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
@@ -990,7 +1010,7 @@ cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nop
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb);
+  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb, 0);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -24,13 +24,14 @@ struct GemvArgs {
   uint32_t* cnt;         // wact counters, zero between calls
   uint32_t* err;         // error bits
   int epi = 0;           // 1: Y = SiLU(gate rows . x) * (up rows . x)
+  int deep = 0;          // 1: deeper per-warp rings, two CTAs per SM (plain products, M <= 2)
 };
 
 constexpr int kStreamWarpsPerCta = 4;
 constexpr int kStreamTileRows = 32;
 int stream_mb_for(int M);                   // staged activation rows: 1, 2, 4 or 8
 int stream_weights_per_unit(int variant);   // 256 (dual) or 512 (single-scale)
-size_t stream_smem_bytes(int variant, int mb);
+size_t stream_smem_bytes(int variant, int mb, int deep);
 cudaError_t stream_prepare(int variant, int act, int mb);  // sets the dynamic smem attribute
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm);
 cudaError_t stream_init_driver();           // resolves cuTensorMapEncodeTiled once
