@@ -145,23 +145,69 @@ RF4_DEV uint32_t quant_scale(float amax) {
   return lo;
 }
 
-// Code of x for half-scale hs (hs > 0): the nearest Codebook10 magnitude, ties
-// to the smaller, sign in bit 3; zero is code 0.
-RF4_DEV uint32_t quant_code(float x, float hs) {
-  const float a = fabsf(x);
-  const uint32_t k = (a > 0.5f * hs) + (a > 1.5f * hs) + (a > 2.5f * hs) + (a > 3.5f * hs) + (a > 5.f * hs) +
-                     (a > 7.f * hs) + (a > 9.f * hs);
-  return k == 0 ? 0u : (x < 0.f ? 8u + k : k);
-}
-
-// Source value of a 16-bit pattern; non-finite values count as 0.
+// Packed source pairs.  Every threshold of the rule, a Codebook10 midpoint
+// (0.5, 1.5, 2.5, 3.5, 5, 7, 9) times a half-scale (at most 4 significant
+// bits, 2^-10 .. 224), has at most 8 significant bits and lies in
+// [2^-11, 2016]: it is exact in fp16 and in bf16, so comparing a source value
+// with it in the source's own 16-bit format is the exact comparison.  Two
+// values are compared per instruction.
 template <int ACT>
-RF4_DEV float quant_src(uint32_t bits) {
-  if constexpr (ACT == 0) {
-    return (bits & 0x7C00u) == 0x7C00u ? 0.f : __half2float(__ushort_as_half((uint16_t)bits));
-  } else {
-    return (bits & 0x7F80u) == 0x7F80u ? 0.f : __uint_as_float(bits << 16);
+struct Pack {
+  // |x| per lane with non-finite lanes set to 0 (they count as 0)
+  static RF4_DEV uint32_t clean_abs(uint32_t w) {
+    const uint32_t a = w & 0x7FFF7FFFu;
+    uint32_t fin;  // 0xFFFF per lane with a <= the largest finite value
+    if constexpr (ACT == 0)
+      asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(fin) : "r"(a), "r"(0x7BFF7BFFu));
+    else
+      asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(fin) : "r"(a), "r"(0x7F7F7F7Fu));
+    return a & fin;
   }
+  // the exactly representable f in both lanes
+  static RF4_DEV uint32_t broadcast(float f) {
+    uint32_t h;
+    if constexpr (ACT == 0)
+      h = __half_as_ushort(__float2half_rn(f));
+    else
+      h = __float_as_uint(f) >> 16;
+    return h | (h << 16);
+  }
+  // per lane: 1 if a > t (a clean, t a threshold), summed onto c
+  static RF4_DEV uint32_t count_gt(uint32_t c, uint32_t a, uint32_t t) {
+    uint32_t g;
+    if constexpr (ACT == 0) {
+      asm("set.gt.f16x2.f16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
+      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(c), "r"(g));
+    } else {
+      asm("set.gt.bf16x2.bf16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
+      asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(c), "r"(g));
+    }
+    return c;
+  }
+  // counts start at 1024 (fp16) / 128 (bf16), where the format's unit in the
+  // last place is 1, so a count k <= 7 sits in the low 3 bits of each lane
+  static constexpr uint32_t kCountBase = ACT == 0 ? 0x64006400u : 0x43004300u;
+  static RF4_DEV float to_f32(uint32_t h) {
+    if constexpr (ACT == 0)
+      return __half2float(__ushort_as_half((uint16_t)h));
+    else
+      return __uint_as_float(h << 16);
+  }
+};
+
+// Codes of the pair w (same scale group) for the thresholds t[0..6] of its
+// half-scale: the nearest Codebook10 magnitude, ties to the smaller, sign in
+// bit 3, zero (and any value that counts as 0) code 0.  Low lane in bits 0-3,
+// high lane in bits 16-19.
+template <int ACT>
+RF4_DEV uint32_t pair_codes(uint32_t w, uint32_t a, const uint32_t (&t)[7]) {
+  uint32_t c = Pack<ACT>::kCountBase;
+#pragma unroll
+  for (int j = 0; j < 7; ++j) c = Pack<ACT>::count_gt(c, a, t[j]);
+  const uint32_t k = c & 0x00070007u;
+  // sign bit 15 / 31 to bit 3 / 19 of the lanes with a nonzero count
+  const uint32_t nz = (k + 0x00070007u) & 0x00080008u;  // bit 3 of a lane set iff its k != 0
+  return k | ((w >> 12) & nz);
 }
 
 template <int V, int ACT>
@@ -185,13 +231,16 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
       for (int i = 0; i < 16; ++i) w[i] = (uint32_t)s[2 * i] | ((uint32_t)s[2 * i + 1] << 16);
     }
     // value i: w[i / 2] half i % 2; scale group 0 = values 0..15, group 1 = 16..31 (dual)
-    float am0 = 0.f, am1 = 0.f;
+    uint32_t a[16];
+    uint32_t m0 = 0, m1 = 0;  // largest |value| bits per group: non-negative values order as their bits
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float lo = fabsf(quant_src<ACT>(w[i] & 0xFFFFu)), hi = fabsf(quant_src<ACT>(w[i] >> 16));
-      if (i < 8) am0 = fmaxf(am0, fmaxf(lo, hi));
-      else am1 = fmaxf(am1, fmaxf(lo, hi));
+      a[i] = Pack<ACT>::clean_abs(w[i]);
+      const uint32_t hi = max(a[i] & 0xFFFFu, a[i] >> 16);
+      if (i < 8) m0 = max(m0, hi);
+      else m1 = max(m1, hi);
     }
+    const float am0 = Pack<ACT>::to_f32(m0), am1 = Pack<ACT>::to_f32(m1);
     uint32_t e0, e1;
     if constexpr (V == 0) {
       e0 = quant_scale(am0);
@@ -200,24 +249,35 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
       e0 = e1 = quant_scale(fmaxf(am0, am1));
     }
     const float hs0 = 0.5f * ue4m3_f32(e0), hs1 = 0.5f * ue4m3_f32(e1);
-    // byte j: value j (low nibble, group 0) and value j + 16 (high nibble, group 1)
-    uint32_t bytes[16];
+    // thresholds: midpoints of the magnitudes {0,1,2,3,4,6,8,10} times the half-scale
+    // (a zero half-scale gives zero thresholds, and a group of zeros gives codes 0)
+    const float mid[7] = {0.5f, 1.5f, 2.5f, 3.5f, 5.f, 7.f, 9.f};
+    uint32_t t0[7], t1[7];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float xl = quant_src<ACT>((w[j / 2] >> (16 * (j % 2))) & 0xFFFFu);
-      const float xh = quant_src<ACT>((w[8 + j / 2] >> (16 * (j % 2))) & 0xFFFFu);
-      const uint32_t cl = hs0 > 0.f ? quant_code(xl, hs0) : 0u, ch = hs1 > 0.f ? quant_code(xh, hs1) : 0u;
-      bytes[j] = cl | (ch << 4);
+    for (int j = 0; j < 7; ++j) {
+      t0[j] = Pack<ACT>::broadcast(mid[j] * hs0);
+      t1[j] = Pack<ACT>::broadcast(mid[j] * hs1);
+    }
+    // byte j: value j (low nibble, group 0) and value j + 16 (high nibble, group 1);
+    // o16[i] = bytes 2i and 2i+1 = codes of values 2i, 2i+16, 2i+1, 2i+17
+    uint32_t o16[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t cl = pair_codes<ACT>(w[i], a[i], t0), ch = pair_codes<ACT>(w[8 + i], a[8 + i], t1);
+      o16[i] = (cl & 0xFu) | ((ch & 0xFu) << 4) | ((cl >> 16) << 8) | ((ch >> 16) << 12);
     }
     uint8_t* out = W + blk * F::BB;
     if constexpr (V == 0) {  // 18-byte blocks start on even addresses: nine 16-bit stores
-      uint16_t* o16 = reinterpret_cast<uint16_t*>(out);
+      uint16_t* p16 = reinterpret_cast<uint16_t*>(out);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o16[k] = (uint16_t)(bytes[2 * k] | (bytes[2 * k + 1] << 8));
-      o16[8] = (uint16_t)(e0 | (e1 << 8));
+      for (int k = 0; k < 8; ++k) p16[k] = (uint16_t)o16[k];
+      p16[8] = (uint16_t)(e0 | (e1 << 8));
     } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) out[j] = (uint8_t)bytes[j];
+      for (int k = 0; k < 8; ++k) {
+        out[2 * k] = (uint8_t)o16[k];
+        out[2 * k + 1] = (uint8_t)(o16[k] >> 8);
+      }
       out[16] = (uint8_t)e0;
     }
   }
