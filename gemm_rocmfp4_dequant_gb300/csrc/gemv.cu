@@ -6,32 +6,36 @@
 // is ROCmFP4?" (Block Layout, Codebook10 Value Table, Scale Format); common.cuh
 // explains how the Blackwell e2m1/e4m3 conversions reproduce it exactly.
 //
-// Work decomposition (stream-K over warps).  The matrix is cut into units of
-// 32 rows x SPAN bytes (8 dual blocks = 144 B, or 16 single-scale blocks =
-// 272 B, per row).  Units are ordered tile-major (all K spans of rows 0..15,
-// then rows 16..31, ...) and every active warp of a persistent grid takes an
-// equal contiguous range of them, so every warp streams the same number of
-// bytes.  A warp streams its units through a private ring of shared-memory
-// stages filled by 1-D bulk copies (one per row, plus one per activation
-// row for the unit's K span), one mbarrier per stage.
+// Work decomposition.  The matrix is cut into units of 32 rows x SPAN bytes
+// (8 dual blocks = 144 B, or 16 single-scale blocks = 272 B, per row).
+// Units are ordered tile-major (all K spans of rows 0..31, then rows 32..63,
+// ...) and every active warp takes an equal contiguous range of them, four
+// warps to a CTA.  The host sizes the grid (api.cu): one CTA per run of whole
+// tiles when that keeps each CTA's weights small (then a tile is split only
+// between the warps of one CTA), else every warp that fits.  A warp streams
+// its units through a private ring of shared-memory stages: one 2-D TMA box
+// of the unit's 32 weight rows plus a bulk copy per activation row of the
+// unit's K span, one mbarrier per stage.  The DEEP instance has a deeper
+// ring (two CTAs per SM) for grids that place at most two CTAs on an SM.
 //
 // Per unit, lane (q = lane/4, c = lane%4) owns rows q, q+8, q+16, q+24 (two
-// m16 tiles that share every B fragment) and the
-// 4-byte-aligned lane span c (BPL whole blocks) of each row.  Each block is
-// eight mma.m16n8k16 steps: step s feeds qs bytes 2s and 2s+1 of the lane's
-// block; each byte becomes one f16x2 A register (low nibble -> weight 2s or
-// 2s+1 of half 0, high nibble -> the weight 16 further on, in half 1),
-// already multiplied by the half-scale pair.  B column n holds activation
-// vector n (zero for n >= M), permuted the same way.  D is flushed into
-// round-to-nearest fp32 registers after every block (8 MMAs), so the tensor
-// core's own accumulation never runs long.
+// m16 tiles that share every B fragment) and the 4-byte-aligned lane span c
+// (BPL whole blocks) of each row.  Each block is eight mma.m16n8k16 steps:
+// step s feeds qs bytes 2s and 2s+1 of the lane's block; each byte becomes
+// one f16x2 A register (low nibble -> weight 2s or 2s+1 of half 0, high
+// nibble -> the weight 16 further on, in half 1).  For M = 1 the 8 B columns
+// hold (block, half) pairs, so each lane receives exact half-block sums and
+// applies the fp32 half-scales once per half; for M > 1, B column n holds
+// activation vector n (zero for n >= M) and the A registers carry the
+// half-scales.  D is flushed into round-to-nearest fp32 registers after every
+// block (8 MMAs), so the tensor core's own accumulation never runs long.
 //
 // A tile (32 rows) whose units are split between warps is finished by its
-// last-arriving warp: each contributor writes its 32 x 8 partial to the
-// workspace, fences, and bumps a per-tile counter; the warp that completes
-// the count sums all partials in warp (= K) order, writes Y and resets the
-// counter.  Nobody waits and the sum order is fixed, so results are bitwise
-// reproducible.
+// last-arriving warp, in two levels: the warps of one CTA meet in shared
+// memory, and CTAs that share a tile write 32 x 8 partials to the workspace,
+// fence, and bump a per-tile counter; the one that completes the count sums
+// all partials in K order, writes Y and resets the counter.  Nobody waits and
+// the sum order is fixed, so results are bitwise reproducible.
 #include <cudaTypedefs.h>
 
 #include <cstring>
