@@ -25,7 +25,7 @@
 // partial (max, sum, P.V) and the combine kernel merges the splits in split
 // order.  Every order is fixed, so results are bitwise repeatable.
 //
-// Byte order inside a block (R1): byte j holds weight j (low nibble) and
+// Byte order inside a block (read as in ggml Q4_0): byte j holds weight j (low nibble) and
 // weight j+16 (high nibble), so cvt.rn.f16x2.e2m1x2 of byte j gives the pair
 // (d = j, d = j + 16) of that block.  Lane (r, c) = (lane / 4, lane % 4)
 // decodes bytes 4c .. 4c+3 of every block of its tokens; the MMA k order is

@@ -1,8 +1,10 @@
-// Elementwise ROCmFP4 kernels: dequantisation, scale validation, and the
-// generic product used when a shape or pointer alignment does not fit the
-// streaming kernel.  Decode follows "Feasibility Report: Porting ROCmFP4 to
-// Atlas", section "What is ROCmFP4?" (Block Layout, Codebook10 Value Table,
-// Scale Format), in plain fp32 arithmetic that is exact for every weight.
+// Elementwise ROCmFP4 kernels: dequantisation, scale validation, the
+// quantiser (fp16 / bf16 -> ROCmFP4 blocks), and the generic product used
+// when a shape or pointer alignment does not fit the streaming kernel.
+// Decode follows "Feasibility Report: Porting ROCmFP4 to Atlas", section
+// "What is ROCmFP4?" (Block Layout, Codebook10 Value Table, Scale Format), in
+// plain fp32 arithmetic that is exact for every weight; the quantiser inverts
+// it with the smallest covering scale and nearest codes, by exact comparisons.
 #include "common.cuh"
 #include "kernels.h"
 
