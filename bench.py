@@ -854,10 +854,39 @@ def run_model(args, world):
     sb = sum(step_bytes([m], v) for m, v in zip(S.mats, S.variants))
     res = dict(value=world * sb * args.steps / t / 1e9, ms_per_step=t / args.steps * 1e3, clocks=clk.summary(),
                tok_s=world * args.steps / t, gpu_launches=len(S.mats) * args.steps, step_bytes=sb,
+               launches_per_step=len(S.mats),
                weight_gb=round(sum(weight_bytes([m], v) for m, v in zip(S.mats, S.variants)) / 1e9, 3))
     del S
     torch.cuda.empty_cache()
     return res
+
+
+def model_object(args, world, hbm, peak_kind):
+    """The whole-model decode step (257 GEMVs, one CUDA graph per token) for the
+    default line: equivalent decode tok/s and GB/s against the HBM copy peak."""
+    r = run_model(argparse.Namespace(steps=args.steps, warmup=args.warmup, layouts=""), world)
+    return {"kernel": "gemv_stream_kernel", "workload": "64 layers x [7168,5120] [5120,6144] [34816,5120] "
+            "[5120,17408] + LM head [152064,5120], dual, batch 1, fresh x fp16 per GEMV",
+            "tok_s": round(r["tok_s"], 1), "GB/s": round(r["value"], 1), "peak": hbm,
+            "frac": round(r["value"] / hbm, 4), "frac_of": f"{peak_kind} HBM copy bandwidth",
+            "ms_per_step": round(r["ms_per_step"], 4), "step_bytes": r["step_bytes"], "weight_gb": r["weight_gb"],
+            "launches_per_step": r["launches_per_step"],
+            "us_per_launch": round(r["ms_per_step"] * 1e3 / r["launches_per_step"], 3),
+            "steps": args.steps, "clocks": r["clocks"]}
+
+
+def run_sweep(args, world, hbm):
+    """The four layer shapes x {dual, single-scale} x M in {1, 2, 4, 8}: GB/s of
+    each variant's layer step (one graph of four launches)."""
+    table = {}
+    for variant in (0, 1):
+        for M in (1, 2, 4, 8):
+            r = run_gemv(argparse.Namespace(steps=max(20, args.steps // 10), warmup=args.warmup), world, hbm,
+                         LAYER, variant=variant, M=M, with_e2e=False)
+            table[f"{'dual' if variant == 0 else 'fast'} M={M}"] = {
+                "GB/s": round(r["value"], 1), "frac": round(r["value"] / hbm, 4),
+                "kernel_GB/s": round(r["achieved"], 1), "per_launch_us": r["per_launch_us"]}
+    return table
 
 
 # ---- main -----------------------------------------------------------------------------------
@@ -984,6 +1013,8 @@ def main():
         line["gpu_launches"] = res["gpu_launches"]
         line["clocks"] = res["clocks"]
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
+        line["model"] = model_object(args, world, hbm, peak_kind)
+        line["sweep"] = run_sweep(args, world, hbm)
         line["gate_up"] = run_gate_up(hbm)
         line["attention"] = run_attention(hbm)
         line["quantize"] = run_quantize(hbm)
@@ -1006,14 +1037,7 @@ def main():
         line.update(tok_s=round(res["tok_s"], 1), gpu_launches=res["gpu_launches"], clocks=res["clocks"],
                     weight_gb=res["weight_gb"], frac_of_hbm_peak=round(res["value"] / hbm, 4))
     elif args.workload == "sweep":
-        table = {}
-        for variant in (0, 1):
-            for M in (1, 2, 4, 8):
-                r = run_gemv(argparse.Namespace(steps=max(20, args.steps // 10), warmup=args.warmup), world, hbm,
-                             LAYER, variant=variant, M=M, with_e2e=False)
-                table[f"{'dual' if variant == 0 else 'fast'} M={M}"] = {
-                    "GB/s": round(r["value"], 1), "kernel_GB/s": round(r["achieved"], 1),
-                    "per_launch_us": r["per_launch_us"]}
+        table = run_sweep(args, world, hbm)
         first = table["dual M=1"]
         line = base_line(args, world, first["GB/s"], "GB/s", 0.0, cfg, "f16")
         line["sweep"] = table

@@ -174,7 +174,7 @@ def test_full_size_layer_matrix_sampled_rows(variant, name):
     rows = np.unique(np.concatenate([[0, 15, 16, N - 17, N - 1], rng.integers(0, N, 120)]))
     Wrows = synth.weights(N, K, variant, seed=0, stream=synth.weight_stream(0, m), rows=rows)
     assert np.array_equal(W.view(N, rb)[t.from_numpy(rows).cuda()].cpu().numpy(), Wrows)
-    for M in (1, 8):
+    for M in (1, 2, 4, 8):
         Xh = synth.activations(M, K, F16, seed=0, stream=synth.act_stream(0, m))
         Y = rf4.gemm(W, upload_x(Xh, F16), N, K, variant).cpu().numpy()
         ref = oracle.gemm(Wrows, Xh, len(rows), K, variant)
