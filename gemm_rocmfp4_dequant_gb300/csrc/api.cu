@@ -98,6 +98,15 @@ rocmfp4_status device_state(DeviceState** out) {
   return ROCMFP4_OK;
 }
 
+// The state of the current device if an allocating entry point has set it
+// up there, else nullptr (never creates it).
+DeviceState* existing_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_dev[dev].ready ? &g_dev[dev] : nullptr;
+}
+
 rocmfp4_status check_shape(int64_t N, int64_t K, int variant) {
   if (!valid_variant(variant)) return fail(ROCMFP4_ERR_INVALID_ARG, "unknown variant");
   if (N < 0 || K < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
@@ -117,7 +126,9 @@ rocmfp4_status check_shape(int64_t N, int64_t K, int variant) {
 // 8 activation rows) every warp that fits takes a share, which keeps more
 // bytes in flight.
 constexpr int64_t kAlignedCtaBytes = 40 * 4608;  // 40 dual units of 32 rows x 256 weights
-int64_t stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t M, int64_t cap) {
+}  // namespace
+
+int64_t rocmfp4::stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t M, int64_t cap) {
   const int64_t units = tiles * nspans;
   const int64_t maxc = cap / kStreamWarpsPerCta;
   const int64_t tpc = (tiles + maxc - 1) / maxc;  // tiles per CTA
@@ -127,6 +138,8 @@ int64_t stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t 
   }
   return units < cap ? units : cap;
 }
+
+namespace {
 
 rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K, int variant,
                        int act, cudaStream_t s) {
@@ -515,21 +528,26 @@ rocmfp4_status rocmfp4_validate(const void* W, int64_t N, int64_t K, rocmfp4_var
 }
 
 uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream) {
-  DeviceState* d = nullptr;
-  if (device_state(&d) != ROCMFP4_OK) return 0xFFFFFFFFu;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t bits = 0;
-  if (cudaMemcpyAsync(&bits, d->err, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return 0xFFFFFFFFu;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return 0xFFFFFFFFu;
-  if (bits != 0) {
-    // A kernel gave up waiting: its split counters may be left set, so clear them.
-    cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
-    cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
-    cudaMemsetAsync(d->gbar, 0, sizeof(uint32_t), s);
-    cudaMemsetAsync(d->tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d->sms), s);
-    cudaStreamSynchronize(s);
+  // The allocating entry points' workspace, only if one exists: the query
+  // itself never creates it.
+  if (DeviceState* d = existing_state()) {
+    if (cudaMemcpyAsync(&bits, d->err, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return 0xFFFFFFFFu;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return 0xFFFFFFFFu;
+    if (bits != 0) {
+      // A kernel gave up waiting: its split counters may be left set, so clear them.
+      cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
+      cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
+      cudaMemsetAsync(d->gbar, 0, sizeof(uint32_t), s);
+      cudaMemsetAsync(d->tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d->sms), s);
+      if (cudaStreamSynchronize(s) != cudaSuccess) return 0xFFFFFFFFu;
+    }
   }
-  return bits;
+  // The allocation-free entry point's fixed array, if it was set up here.
+  uint32_t nb = 0;
+  if (noalloc_error_bits(s, &nb) != cudaSuccess) return 0xFFFFFFFFu;
+  return bits | nb;
 }
 
 const char* rocmfp4_status_string(rocmfp4_status status) {

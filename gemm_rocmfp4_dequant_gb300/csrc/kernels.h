@@ -36,6 +36,14 @@ cudaError_t stream_prepare(int variant, int act, int mb);  // sets the dynamic s
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm);
 cudaError_t stream_init_driver();           // resolves cuTensorMapEncodeTiled once
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s);
+// Active warps of a single-product streaming launch over `tiles` tiles of
+// `nspans` units of `unit_bytes` weight bytes, M activation rows, with room
+// for `cap` warps (api.cu).
+int64_t stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t M, int64_t cap);
+// Error bits of the allocation-free entry point's fixed scratch on the
+// current device (noalloc.cu): 0 when it has not been set up there.  Reads
+// and clears them, and on a non-zero result zeroes its split counters.
+cudaError_t noalloc_error_bits(cudaStream_t s, uint32_t* bits);
 // Up to kChainOps products with the same variant, activation type, M and
 // wact, in order, in one cooperative launch with a grid barrier after each
 // product (gbar: a zeroed counter).

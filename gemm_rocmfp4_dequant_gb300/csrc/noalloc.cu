@@ -2,16 +2,19 @@
 // not allocate device memory.
 //
 // Some callers cannot call cudaMalloc at the point where they run the
-// product: an engine that has handed all device memory to its own pool, code
-// running while a CUDA graph is being captured, or a host that forbids
-// allocation after start-up.  The regular entry points allocate a per-device
-// workspace on first use; this one never does.  Its scratch -- the
-// split-tile partial sums, their hand-off counters and the error word of the
-// streaming kernel -- lives in the file-scope array below, which every GPU
-// that loads the library holds until the process exits.
+// product: an inference engine that hands all device memory to its own pool
+// at start-up (an allocation behind its back could fail or fragment the
+// memory it planned), a host with a real-time or certification rule against
+// allocating after initialisation (allocation time is unbounded), or a
+// plug-in loaded into a process whose allocator it must not touch.  The
+// regular entry points allocate a per-device workspace on first use; this one
+// never does.  Its scratch -- the split-tile partial sums, their hand-off
+// counters and the error word of the streaming kernel -- lives in the
+// file-scope array below, which every GPU that loads the library holds until
+// the process exits.
 //
-// The paper has no counterpart to this entry point: it is a deployment
-// convenience of this library.
+// The format definition has no counterpart to this entry point: it is a
+// deployment convenience of this library.
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -97,6 +100,35 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+// Reads (and clears) the error word of the array on the current device; a
+// set word means a kernel gave up waiting and may have left split counters
+// raised, so those are zeroed too.  A device without set-up has nothing to
+// report.  Allocates nothing.
+cudaError_t rocmfp4::noalloc_error_bits(cudaStream_t s, uint32_t* bits) {
+  *bits = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].ready) scratch = g_dev[dev].scratch;
+  }
+  if (scratch == nullptr) return cudaSuccess;
+  uint32_t v = 0;
+  if ((e = cudaMemcpyAsync(&v, scratch + kRecordsBytes + kCountersBytes, sizeof(v), cudaMemcpyDeviceToHost, s)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  if (v != 0) {
+    if ((e = cudaMemsetAsync(scratch + kRecordsBytes, 0, kCountersBytes + 256, s)) != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  }
+  *bits = v;
+  return cudaSuccess;
+}
+
 extern "C" rocmfp4_status rocmfp4_gemm_noalloc(const void* W, const void* X, float* Y, int64_t M, int64_t N,
                                                int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                                rocmfp4_stream_t stream) {
@@ -128,7 +160,9 @@ extern "C" rocmfp4_status rocmfp4_gemm_noalloc(const void* W, const void* X, flo
   const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
   int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
   if (cap > kMaxWarps) cap = kMaxWarps;  // the scratch holds records for kMaxWarps warps
-  const int64_t wact = units < cap ? units : cap;
+  // the work split of rocmfp4_gemm_ex, within the array's capacity
+  const int64_t tiles = (N + kStreamTileRows - 1) / kStreamTileRows;
+  const int64_t wact = stream_warps(tiles, K / ku, ku * (variant == ROCMFP4_DUAL ? 18 : 17), M, cap);
   GemvArgs a{};
   a.W = static_cast<const uint8_t*>(W);
   a.X = static_cast<const uint16_t*>(X);
@@ -144,6 +178,7 @@ extern "C" rocmfp4_status rocmfp4_gemm_noalloc(const void* W, const void* X, flo
   a.cnt = reinterpret_cast<uint32_t*>(d->scratch + kRecordsBytes);
   a.err = reinterpret_cast<uint32_t*>(d->scratch + kRecordsBytes + kCountersBytes);
   const int ctas = (int)((wact + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
+  a.deep = mb <= 2 && ctas <= 2 * d->sms ? 1 : 0;
   cudaError_t e = launch_gemv_stream(variant, act, a, ctas, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "streaming kernel launch");
   count_launch();

@@ -214,9 +214,12 @@ rocmfp4_status rocmfp4_gemv_chain_mixed(const rocmfp4_gemv_op *ops, const rocmfp
 /* Y = X . W^T for M <= 8 without allocating device memory.
  *
  * For callers that cannot call cudaMalloc where they run the product: an
- * engine that has given all device memory to its own pool, code running
- * during CUDA graph capture, or a host that forbids allocation after start-up.
- * The paper has no counterpart; this is a deployment convenience.
+ * inference engine that hands all device memory to its own pool at start-up
+ * (a cudaMalloc behind its back could fail, or fragment the memory it
+ * planned), a host with a real-time or certification rule against
+ * allocating after initialisation (allocation time is unbounded), or a
+ * plug-in loaded into a process whose allocator it must not touch.  The
+ * format definition has no counterpart; this is a deployment convenience.
  *
  * Same arguments, layouts and results as rocmfp4_gemm_ex (fp32 Y, fp16 or
  * bf16 X), computed by the same streaming kernel, whose scratch (split-tile
@@ -230,9 +233,13 @@ rocmfp4_status rocmfp4_gemv_chain_mixed(const rocmfp4_gemv_op *ops, const rocmfp
  *   - The first call on a device looks up the array's device address and
  *     zeroes its counters (a cudaMemset and a device synchronisation, no
  *     allocation); make that first call before any stream capture.
- *   - Every call shares the one array per device: calls that overlap on the
- *     GPU (different streams, or graphs replayed concurrently) race and give
- *     wrong results.  Calls ordered on one stream are safe. */
+ *   - Every call shares the one array per device and finds it as the last
+ *     call left it: calls that overlap on the GPU (for instance on two
+ *     unordered streams) race and give wrong results.  Calls ordered on one
+ *     stream are safe.
+ *   - A kernel that gave up waiting records it in the array's own error word;
+ *     rocmfp4_device_error_bits reports and clears it (and the array's
+ *     counters) without allocating. */
 rocmfp4_status rocmfp4_gemm_noalloc(const void *W, const void *X, float *Y, int64_t M, int64_t N,
                                     int64_t K, rocmfp4_variant variant, rocmfp4_act act,
                                     rocmfp4_stream_t stream);
@@ -272,8 +279,11 @@ rocmfp4_status rocmfp4_validate(const void *W, int64_t N, int64_t K, rocmfp4_var
 
 /* Error bits recorded by kernels on the current device since the last query
  * (bit 0: a kernel gave up waiting for its own bulk copies, so its outputs
- * are invalid).  Synchronises with the stream, clears the bits, and on a
- * non-zero result also clears the split-reduction counters.  Returns
+ * are invalid), from the workspace of the allocating entry points and from
+ * the fixed array of rocmfp4_gemm_noalloc, whichever exist on the device.
+ * Synchronises with the stream, clears the bits, and on a non-zero result
+ * also clears the split-reduction counters.  Allocates nothing: a device on
+ * which no allocating entry point has run yet keeps no workspace.  Returns
  * 0xFFFFFFFF if the query itself failed. */
 uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream);
 
