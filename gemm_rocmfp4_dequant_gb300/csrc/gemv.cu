@@ -77,10 +77,12 @@ constexpr int stages() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
+constexpr int kZeroBytes = 256;  // zero activations for lanes whose B column is unused
+
 template <int V, int MB, int DEEP = 0>
 constexpr size_t smem_bytes() {
   return (size_t)kWarps * stages<V, MB, DEEP>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB, DEEP>() * 8 +
-         16 + cta_red_bytes<MB>();
+         16 + cta_red_bytes<MB>() + kZeroBytes;
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -279,14 +281,26 @@ RF4_DEV bool grid_barrier(uint32_t* gbar, uint32_t gen, uint32_t ctas, uint32_t 
 }
 
 // Adds one unit's products into acc (see the kernel comment for the layouts).
+// Lanes whose B column carries no activations read theirs from `zero`, a
+// 256-byte page of zeros in shared memory, so every lane runs the same loads.
 template <int V, int ACT, int MB>
-RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2][4]) {
+RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2][4], const uint4* zero) {
   using F = Fmt<V>;
   constexpr int SW = F::SW;
   constexpr int XROW = F::KU * 2;
   const int q = lane >> 2, c = lane & 3;
-  const bool bcol = q < M;  // this lane holds B column q (activation row q)
-  const uint4* xs = reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + (bcol ? q : 0) * XROW);
+  const uint8_t* sb = stage + c * F::LANE_BYTES;
+  // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span,
+  // loaded inside each block's step (only that block's words stay live)
+  auto load_words = [&](uint32_t (&w0)[SW], uint32_t (&w1)[SW], uint32_t (&w2)[SW], uint32_t (&w3)[SW]) {
+#pragma unroll
+    for (int k = 0; k < SW; ++k) {
+      w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
+      w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
+      w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
+      w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+    }
+  };
   if constexpr (MB == 1) {
     // M == 1, column split: B column n = 2c' + h holds x only for the k rows
     // of lane c''s block and half h, so D[row][2c + h] is the half-block sum
@@ -297,37 +311,26 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
     const bool bact = (q >> 1) == c;
     const uint32_t sel0 = !bact ? 0x4444u : (hb ? 0x1044u : 0x4410u);  // (x[2s], 0) or (0, x[2s+16])
     const uint32_t sel1 = !bact ? 0x4444u : (hb ? 0x3244u : 0x4432u);  // (x[2s+1], 0) or (0, x[2s+17])
+    // the 16 activations of half hb of block c*BPL + phi at xp[phi * 4 + 0..1]
+    const uint4* xp = bact ? reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN) + c * F::BPL * 4 + 2 * hb
+                           : zero;
 #pragma unroll
     for (int phi = 0; phi < F::BPL; ++phi) {
-      // the 16 activations of half hb of the lane's block (zeros if inactive)
-      uint32_t xh[8];
-      if (bact) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const uint4 v = xs[(c * F::BPL + phi) * 4 + 2 * hb + k];
-          xh[4 * k] = v.x;
-          xh[4 * k + 1] = v.y;
-          xh[4 * k + 2] = v.z;
-          xh[4 * k + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xh[k] = 0u;
-      }
       uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
-      const uint8_t* sb = stage + c * F::LANE_BYTES;
+      load_words(w0, w1, w2, w3);
+      uint32_t xh[8];
 #pragma unroll
-      for (int k = 0; k < SW; ++k) {
-        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
-        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
-        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
-        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      for (int k = 0; k < 2; ++k) {
+        const uint4 v = xp[phi * 4 + k];
+        xh[4 * k] = v.x;
+        xh[4 * k + 1] = v.y;
+        xh[4 * k + 2] = v.z;
+        xh[4 * k + 3] = v.w;
       }
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      float d0[4], d1[4];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int pos = phi * F::BB + 2 * s;
-        // (x[2s] or x[2s+16], 0) / (0, ...) as selected for this lane; zeros if inactive
         const uint32_t b0 = __byte_perm(xh[s], 0u, sel0);
         const uint32_t b1 = __byte_perm(xh[s], 0u, sel1);
         uint32_t a[4];
@@ -335,12 +338,14 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
         a[1] = code_pair<ACT>(e2m1x2_at(w1, pos));
         a[2] = code_pair<ACT>(e2m1x2_at(w0, pos + 1));
         a[3] = code_pair<ACT>(e2m1x2_at(w1, pos + 1));
-        mma16816(d0, a, b0, b1, ACT == 1);
+        if (s == 0) mma16816_z(d0, a, b0, b1, ACT == 1);
+        else mma16816(d0, a, b0, b1, ACT == 1);
         a[0] = code_pair<ACT>(e2m1x2_at(w2, pos));
         a[1] = code_pair<ACT>(e2m1x2_at(w3, pos));
         a[2] = code_pair<ACT>(e2m1x2_at(w2, pos + 1));
         a[3] = code_pair<ACT>(e2m1x2_at(w3, pos + 1));
-        mma16816(d1, a, b0, b1, ACT == 1);
+        if (s == 0) mma16816_z(d1, a, b0, b1, ACT == 1);
+        else mma16816(d1, a, b0, b1, ACT == 1);
       }
       // E4M3 values of the scales of the lane's block, rows q, q+8, q+16, q+24
       const float2 e0 = scale_pair_f32<V>(w0, phi), e1 = scale_pair_f32<V>(w1, phi);
@@ -357,33 +362,23 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
   } else {
     // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or
     // 32 MMAs) and is then flushed into round-to-nearest fp32 registers.
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    // Lane (q, c) holds B column q: activation row q, or zeros for q >= M.
+    const uint4* xp = q < M ? reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + q * XROW) + c * F::BPL * 4
+                            : zero;
+    float d0[4], d1[4];
 #pragma unroll
     for (int phi = 0; phi < F::BPL; ++phi) {
       // 32 activations of the lane's block (block c*BPL + phi of the unit)
-      uint32_t xv[16];
-      if (bcol) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = xs[(c * F::BPL + phi) * 4 + k];
-          xv[4 * k] = v.x;
-          xv[4 * k + 1] = v.y;
-          xv[4 * k + 2] = v.z;
-          xv[4 * k + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) xv[k] = 0u;
-      }
-      // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span
       uint32_t w0[SW], w1[SW], w2[SW], w3[SW];
-      const uint8_t* sb = stage + c * F::LANE_BYTES;
+      load_words(w0, w1, w2, w3);
+      uint32_t xv[16];
 #pragma unroll
-      for (int k = 0; k < SW; ++k) {
-        w0[k] = reinterpret_cast<const uint32_t*>(sb + q * F::SPAN)[k];
-        w1[k] = reinterpret_cast<const uint32_t*>(sb + (q + 8) * F::SPAN)[k];
-        w2[k] = reinterpret_cast<const uint32_t*>(sb + (q + 16) * F::SPAN)[k];
-        w3[k] = reinterpret_cast<const uint32_t*>(sb + (q + 24) * F::SPAN)[k];
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = xp[phi * 4 + k];
+        xv[4 * k] = v.x;
+        xv[4 * k + 1] = v.y;
+        xv[4 * k + 2] = v.z;
+        xv[4 * k + 3] = v.w;
       }
       const uint32_t s0 = scale_pair_at<V>(w0, phi), s1 = scale_pair_at<V>(w1, phi);
       const uint32_t s2 = scale_pair_at<V>(w2, phi), s3 = scale_pair_at<V>(w3, phi);
@@ -398,12 +393,14 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
         a[1] = weight_pair<ACT>(e2m1x2_at(w1, pos), s1);
         a[2] = weight_pair<ACT>(e2m1x2_at(w0, pos + 1), s0);
         a[3] = weight_pair<ACT>(e2m1x2_at(w1, pos + 1), s1);
-        mma16816(d0, a, b0, b1, ACT == 1);
+        if (phi == 0 && s == 0) mma16816_z(d0, a, b0, b1, ACT == 1);
+        else mma16816(d0, a, b0, b1, ACT == 1);
         a[0] = weight_pair<ACT>(e2m1x2_at(w2, pos), s2);
         a[1] = weight_pair<ACT>(e2m1x2_at(w3, pos), s3);
         a[2] = weight_pair<ACT>(e2m1x2_at(w2, pos + 1), s2);
         a[3] = weight_pair<ACT>(e2m1x2_at(w3, pos + 1), s3);
-        mma16816(d1, a, b0, b1, ACT == 1);
+        if (phi == 0 && s == 0) mma16816_z(d1, a, b0, b1, ACT == 1);
+        else mma16816(d1, a, b0, b1, ACT == 1);
       }
     }
 #pragma unroll
@@ -707,6 +704,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
   CtaRed red;
   red.rec = reinterpret_cast<float*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + 16);
   red.cnt = reinterpret_cast<uint32_t*>(red.rec + kWarps * 2 * kTileRows * MB);  // used only if cta_red_bytes<MB>() > 0
+  uint4* zero = reinterpret_cast<uint4*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + 16 +
+                                         cta_red_bytes<MB>());
+  if (threadIdx.x < kZeroBytes / 16) zero[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   const int64_t cta_first = (int64_t)blockIdx.x * kWarps;
   const uint32_t warps_here = (uint32_t)(wact - cta_first < kWarps ? wact - cta_first : kWarps);
   const uint32_t ctas = (uint32_t)((wact + kWarps - 1) / kWarps);
@@ -724,6 +724,81 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
     fence_mbar_init();
   }
   __syncwarp();
+
+  if constexpr (NOPS == 1) {
+    // A single product: this warp's units u0 .. u1 - 1, tile-major.  Weights
+    // of up to NS - 1 units are requested before the dependency wait; after
+    // it, each unit's activations go out with (or right after) its weights.
+    const StreamOp& op = p.op[0];
+    const int S = (int)op.nspans;
+    const int64_t u0 = op.units * wg / wact, u1 = op.units * (wg + 1) / wact;
+    const int n = (int)(u1 - u0);
+    int tw = (int)(u0 / S), jw = (int)(u0 % S), jx = jw;
+    int iw = 0, ix = 0, sw = 0, sx = 0;  // units issued (weights, activations) and their stages
+    auto issue_w1 = [&]() {
+      issue_w<V, MB, EPI>(&op.tmw, M, tw, jw, ring + (size_t)sw * SB, smem_addr(&bars[sw]), lane);
+      if (++jw == S) {
+        jw = 0;
+        ++tw;
+      }
+      if (++sw == NS) sw = 0;
+      ++iw;
+    };
+    auto issue_x1 = [&]() {
+      issue_x<V, MB>(op.X, op.K, M, jx, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
+      if (++jx == S) jx = 0;
+      if (++sx == NS) sx = 0;
+      ++ix;
+    };
+    while (iw < NS - 1 && iw < n) issue_w1();
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __syncwarp();
+    while (ix < iw) issue_x1();
+
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    int t = (int)(u0 / S), j = (int)(u0 % S), js = j;
+    int k = 0, st = 0;
+    uint32_t phase = 0;
+    bool failed = false;
+    for (; k < n; ++k) {
+      if (iw < n) {  // unit k + NS - 1 goes into the stage unit k - 1 has released
+        issue_w1();
+        issue_x1();
+      }
+      if (!mbar_wait_bounded(smem_addr(&bars[st]), phase)) {
+        failed = true;
+        break;
+      }
+      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
+      __syncwarp();
+      fence_proxy_async();
+      if (j == S - 1 || k == n - 1) {
+        finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
+        js = 0;
+      }
+      if (++j == S) {
+        j = 0;
+        ++t;
+      }
+      if (++st == NS) {
+        st = 0;
+        phase ^= 1u;
+      }
+    }
+    if (failed) {
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      // every armed stage has its activation copies issued (ix == iw); let all copies land
+      for (; k < iw; ++k) {
+        (void)mbar_wait_bounded(smem_addr(&bars[st]), phase);
+        if (++st == NS) {
+          st = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    return;
+  }
 
   // cw: next unit whose weights to copy (unit index iw of this warp);
   // cx: next unit whose activations to copy (ix <= iw); activations of
@@ -789,7 +864,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
         failed = true;
         break;
       }
-      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc);
+      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
       __syncwarp();
       fence_proxy_async();
       if (j == Si - 1 || k == nunits - 1) {

@@ -252,5 +252,6 @@ def test_attention_key_rows_every_code_and_scale(variant):
     assert np.all(err <= lim), f"|err| {err[worst]:.3e} > {lim[worst[0], worst[1], 0]:.3e} at {worst}"
     # the scores of the large-scale sequences are far from uniform, so a wrong K decode shows
     Kd = oracle.dequant(Kc, B * Hkv * Tmax, D, variant).reshape(B, Hkv, Tmax, D)
-    scores = scale * Kd[NSCALE - 1, 0] @ synth.bits_to_float(qh[NSCALE - 1, 0], F16)
-    assert np.ptp(scores) > 2  # softmax weights spread over a factor e^2 or more
+    spread = max(np.ptp(scale * Kd[NSCALE - 1, h // G] @ synth.bits_to_float(qh[NSCALE - 1, h], F16))
+                 for h in range(H))
+    assert spread > 2  # some head's softmax weights spread over a factor e^2 or more
