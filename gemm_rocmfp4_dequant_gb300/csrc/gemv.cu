@@ -800,29 +800,28 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
     return;
   }
 
-  // cw: next unit whose weights to copy (unit index iw of this warp);
-  // cx: next unit whose activations to copy (ix <= iw); activations of
-  // product g may be read once g <= readable.
+  // A chain.  cw: next unit whose weights to copy (the iw-th of this warp,
+  // into stage sw); cx: next unit whose activations to copy (ix <= iw, stage
+  // sx); activations of product g may be read once g <= readable.  Weights
+  // never depend on earlier work, so the ring stays full across products.
   Cursor cw, cx;
   cursor_begin(cw, p, 0, wg);
   cx = cw;
-  int iw = 0, ix = 0, readable = 0;
+  int iw = 0, ix = 0, sw = 0, sx = 0, readable = 0;
   auto issue_w_next = [&]() {
-    const int st = iw % NS;
-    issue_w<V, MB, EPI>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
+    issue_w<V, MB, EPI>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)sw * SB, smem_addr(&bars[sw]), lane);
     const int g0 = cw.g;
     ++iw;
+    if (++sw == NS) sw = 0;
     cursor_next(cw, p, wg);
     if (cw.g != g0 && cw.g < p.nops && lane == 0)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.op[cw.g].tmw)) : "memory");
   };
-  auto issue_x_ready = [&]() {
-    while (ix < iw && cx.g <= readable) {
-      const int st = ix % NS;
-      issue_x<V, MB>(p.op[cx.g].X, p.op[cx.g].K, M, cx.j, ring + (size_t)st * SB, smem_addr(&bars[st]), lane);
-      ++ix;
-      cursor_next(cx, p, wg);
-    }
+  auto issue_x_next = [&]() {
+    issue_x<V, MB>(p.op[cx.g].X, p.op[cx.g].K, M, cx.j, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
+    ++ix;
+    if (++sx == NS) sx = 0;
+    cursor_next(cx, p, wg);
   };
 
   // Start streaming weights, then wait for the preceding grid before
@@ -831,10 +830,11 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
   grid_dependency_wait();
   grid_launch_dependents();
   __syncwarp();
-  issue_x_ready();
+  while (ix < iw && cx.g <= readable) issue_x_next();
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  int i = 0;  // this warp's unit being computed
+  int i = 0, st = 0;  // this warp's unit being computed, its stage and the stage's phase
+  uint32_t phase = 0;
   bool failed = false;
   for (int g = 0; g < p.nops && !failed; ++g) {
     if (g > 0) {
@@ -845,35 +845,38 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
         break;
       }
       readable = g;
-      issue_x_ready();
+      while (ix < iw && cx.g <= readable) issue_x_next();
     }
     const StreamOp& op = p.op[g];
-    const int64_t U = op.units, S = op.nspans;
     if (wg >= op.wact) continue;
+    const int64_t U = op.units;
+    const int S = (int)op.nspans;
     const int64_t u0 = U * wg / op.wact, u1 = U * (wg + 1) / op.wact;
     const int nunits = (int)(u1 - u0);
-    const int t_first = (int)(u0 / S), Si = (int)S;
-    int t = t_first, j = (int)(u0 % S), js = j;
+    int t = (int)(u0 / S), j = (int)(u0 % S), js = j;
     for (int k = 0; k < nunits; ++k, ++i) {
-      // keep NS - 1 units in flight ahead of the one being computed
-      while (iw < i + NS && cw.g < p.nops) issue_w_next();
-      __syncwarp();
-      issue_x_ready();
-      const int st = i % NS;
-      if (!mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / NS) & 1))) {
+      // keep NS units in flight, counting the one being computed; a unit's
+      // activations follow its weights once its product is readable
+      if (iw < i + NS && cw.g < p.nops) issue_w_next();
+      if (ix < iw && cx.g <= readable) issue_x_next();
+      if (!mbar_wait_bounded(smem_addr(&bars[st]), phase)) {
         failed = true;
         break;
       }
       compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
       __syncwarp();
       fence_proxy_async();
-      if (j == Si - 1 || k == nunits - 1) {
+      if (j == S - 1 || k == nunits - 1) {
         finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
         js = 0;
       }
-      if (++j == Si) {
+      if (++j == S) {
         j = 0;
         ++t;
+      }
+      if (++st == NS) {
+        st = 0;
+        phase ^= 1u;
       }
     }
   }
@@ -884,8 +887,14 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
     // read) and let all copies land before the shared memory is released.
     readable = p.nops;
     __syncwarp();
-    issue_x_ready();
-    for (int k = i; k < iw; ++k) (void)mbar_wait_bounded(smem_addr(&bars[k % NS]), (uint32_t)((k / NS) & 1));
+    while (ix < iw) issue_x_next();
+    for (; i < iw; ++i) {
+      (void)mbar_wait_bounded(smem_addr(&bars[st]), phase);
+      if (++st == NS) {
+        st = 0;
+        phase ^= 1u;
+      }
+    }
   } else if (p.nops > 1) {
     // Exit arrival: the CTA's last warp arrives once more on the grid counter
     // (every CTA arrives nops times in all); the final arrival of the grid
