@@ -361,6 +361,24 @@ def time_steps(step_fn, steps, warmup, world):
     return a.elapsed_time(b) / 1e3
 
 
+def time_runs(run_fn, steps, warmup, world):
+    """As time_steps, for a run_fn(n, first) that performs n consecutive steps."""
+    import torch
+    run_fn(warmup, 0)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    run_fn(steps, warmup)
+    b.record(s)
+    b.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    return a.elapsed_time(b) / 1e3
+
+
 class L2Flush:
     """A buffer larger than L2; writing it evicts whatever an earlier call left in L2."""
 
@@ -422,7 +440,25 @@ class GemvStep:
             with torch.cuda.graph(g):
                 self.run(r)
             self.graphs.append(g)
+        # one pass per resident copy in one graph, as an engine captures many layers per token
+        self.multi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.multi):
+            for r in range(self.copies):
+                self.run(r)
         torch.cuda.synchronize()
+
+    def run_steps(self, n, first):
+        """n consecutive passes starting at pass `first` (copy first % copies): whole
+        rotations from the multi-pass graph, the rest from single-pass graphs."""
+        i = 0
+        while i < n:
+            r = (first + i) % self.copies
+            if r == 0 and i + self.copies <= n:
+                self.multi.replay()
+                i += self.copies
+            else:
+                self.graphs[r].replay()
+                i += 1
 
     def launches_per_step(self):
         return len(self.mats)
@@ -438,7 +474,7 @@ def per_matrix_kernel_times(L: GemvStep, reps=None):
     of that matrix's product (rotating over the resident copies, so every launch
     streams from HBM) is replayed between CUDA events on the launching stream."""
     import torch
-    reps = reps or max(8, 2 * L.copies)
+    reps = reps or max(20, 2 * L.copies)
     out = []
     for m, (name, N, K) in enumerate(L.mats):
         g = torch.cuda.CUDAGraph()
@@ -496,7 +532,7 @@ def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True):
     L.capture()
     launches0 = L.rf4.launch_count()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        t = time_steps(lambda i: L.graphs[i % copies].replay(), args.steps, args.warmup, world)
+        t = time_runs(L.run_steps, args.steps, args.warmup, world)
     t = max_over_ranks(t, world)
     sb = step_bytes(mats, variant, M)
     kt = per_matrix_kernel_times(L)
@@ -956,6 +992,8 @@ def main():
     ap.add_argument("--layouts", default="", help="model workload: block layout per tensor role, "
                     "e.g. qkv=dual,o=dual,gate_up=fast,down=fast,lm_head=dual (default: all dual)")
     ap.add_argument("--no-prefill", action="store_true", help="leave the prefill object out of the layer line")
+    ap.add_argument("--no-model", action="store_true", help="leave the whole-model object out of the layer line")
+    ap.add_argument("--no-sweep", action="store_true", help="leave the variant sweep out of the layer line")
     ap.add_argument("--prefill-m", type=str, default=",".join(str(m) for m in PREFILL_M),
                     help="comma-separated token counts of the prefill GEMM")
     args = ap.parse_args()
@@ -1007,14 +1045,18 @@ def main():
         res = run_gemv(args, world, hbm, LAYER)
         cfg["l2"] = (f"rotating {res['copies']} resident layer copies ({res['footprint_gb']} GB > 129 MB L2); "
                      "inputs larger than L2")
+        cfg["graphs"] = (f"one CUDA graph holds one layer pass per resident copy ({res['copies']} passes, "
+                         f"{4 * res['copies']} PDL launches); steps replay it")
         line = base_line(args, world, res["value"], "GB/s", res["ms_per_step"], cfg, "f16")
         line["roofline"] = gemv_roofline(res, hbm, peak_kind, LAYER, 0, 1)
         line["e2e"] = res["e2e"]
         line["gpu_launches"] = res["gpu_launches"]
         line["clocks"] = res["clocks"]
         line["frac_of_hbm_peak"] = round(res["value"] / hbm, 4)
-        line["model"] = model_object(args, world, hbm, peak_kind)
-        line["sweep"] = run_sweep(args, world, hbm)
+        if not args.no_model:
+            line["model"] = model_object(args, world, hbm, peak_kind)
+        if not args.no_sweep:
+            line["sweep"] = run_sweep(args, world, hbm)
         line["gate_up"] = run_gate_up(hbm)
         line["attention"] = run_attention(hbm)
         line["quantize"] = run_quantize(hbm)
