@@ -9,7 +9,9 @@ the softmax weights then carry a relative error of at most ln 2 * dx each (the
 max is subtracted exactly), and the weighted sum adds a few 1e-7 relative
 (P split into two fp16 parts, fp32 sums).  Each output element is a convex
 combination of V rows, so
-    |d out| <= (2 ln2 dx + 4e-6) * max |V|   (over the sequence's rows and D).
+    |d out| <= (2 ln2 dx + 4e-6) * max |V|   (over the sequence's rows and D),
+and the whole output is held to relative L2 error 1e-5, the bar of every
+product here.
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ import pytest
 import gemm_rocmfp4_dequant_gb300 as rf4
 import oracle
 import synth
-from gpu_util import torch, upload_w, upload_x
+from gpu_util import REL_L2, torch, upload_w, upload_x
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +76,10 @@ def run_and_check(B, H, Hkv, D, Tmax, lens, scale, variant, act, seed, what=""):
     err = np.abs(got - ref)
     worst = np.unravel_index(np.argmax(err - lim), err.shape)
     assert np.all(err <= lim), f"{what}: |err| {err[worst]:.3e} > {lim[worst[0], worst[1], 0]:.3e} at {worst}"
+    nref = np.linalg.norm(ref)
+    if nref > 0:  # the relative L2 bar of every product in this library
+        rel = np.linalg.norm(got - ref) / nref
+        assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e} > {REL_L2}"
     return got, ref, err
 
 
