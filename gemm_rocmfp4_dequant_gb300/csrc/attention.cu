@@ -332,10 +332,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
         const int alc = row_align<V, D>(kb * F::BB), als = row_align<V, D>(kb * F::BB + 16);
         decode4(lds_bytes4_al(ra + kb * F::BB + 4 * c, alc), block_scales<V>(ra + kb * F::BB, als), va);
         decode4(lds_bytes4_al(rb + kb * F::BB + 4 * c, alc), block_scales<V>(rb + kb * F::BB, als), vb);
+        if (t0 + kChunk > T) {  // only the last chunk has tokens past the sequence
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // tokens past the sequence: zeros (their rows are not data)
-          va[k] = ta < T ? va[k] : 0u;
-          vb[k] = tb < T ? vb[k] : 0u;
+          for (int k = 0; k < 4; ++k) {  // tokens past the sequence: zeros (their rows are not data)
+            va[k] = ta < T ? va[k] : 0u;
+            vb[k] = tb < T ? vb[k] : 0u;
+          }
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
