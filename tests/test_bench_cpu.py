@@ -119,3 +119,30 @@ def test_replicas_take_the_max_over_ranks():
     out = mgr.dict()
     mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True, start_method="spawn")
     assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_layer_passes_replay_whole_rotations_and_count_exactly():
+    """run_steps(n, first) replays exactly n passes, copy (first + i) % copies for
+    pass i: whole rotations from the multi-pass graph, the rest one by one."""
+    import bench
+
+    class G:
+        def __init__(self, log, tag):
+            self.log, self.tag = log, tag
+
+        def replay(self):
+            self.log.append(self.tag)
+
+    for copies in (2, 3, 4):
+        for first in range(0, 2 * copies + 1):
+            for n in range(0, 3 * copies + 2):
+                log = []
+                step = type("S", (), {})()
+                step.copies = copies
+                step.multi = G(log, "multi")
+                step.graphs = [G(log, r) for r in range(copies)]
+                bench.GemvStep.run_steps(step, n, first)
+                passes = []
+                for tag in log:
+                    passes.extend(range(copies) if tag == "multi" else [tag])
+                assert passes == [(first + i) % copies for i in range(n)], (copies, first, n, log)
