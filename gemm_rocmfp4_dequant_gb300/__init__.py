@@ -88,31 +88,54 @@ def _check(status: int, where: str) -> None:
         raise RocmFP4Error(status, where, msg)
 
 
+_torch_mod = None
+_raw_stream = None  # (current device, raw current stream of a device), when torch exposes them
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+    return _torch_mod
+
+
+def _current_stream() -> int:
+    """Handle of torch's current CUDA stream on the current device.  The public
+    torch.cuda.current_stream() builds a Stream object per call (about 3 us on
+    the host); torch's raw accessors give the same handle without it."""
+    global _raw_stream
+    torch = _torch()
+    if _raw_stream is None:
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream = (get_dev, get_raw) if get_dev and get_raw else False
+    if _raw_stream:
+        return _raw_stream[1](_raw_stream[0]())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _stream(stream):
-    torch = _torch()
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return _current_stream()
+    torch = _torch()
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _act_of(t) -> int:
     torch = _torch()
-    if t.dtype == torch.float16:
+    dt = t.dtype
+    if dt == torch.float16:
         return ACT_F16
-    if t.dtype == torch.bfloat16:
+    if dt == torch.bfloat16:
         return ACT_BF16
-    raise TypeError(f"activations must be float16 or bfloat16, got {t.dtype}")
+    raise TypeError(f"activations must be float16 or bfloat16, got {dt}")
 
 
-def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+def _ptr(t) -> int:
+    return t.data_ptr() if t is not None and t.numel() > 0 else 0
 
 
 def block_bytes(variant: int) -> int:
@@ -123,11 +146,19 @@ def row_bytes(K: int, variant: int) -> int:
     return int(load().rocmfp4_row_bytes(K, variant))
 
 
+def _row_bytes_fast(K: int, variant: int) -> int:
+    # the layouts' arithmetic (18- or 17-byte blocks of 32 weights); anything
+    # else goes to the library, which rejects it
+    if (variant == DUAL or variant == FAST) and K >= 0 and K % 32 == 0:
+        return (K // 32) * (18 if variant == DUAL else 17)
+    return row_bytes(K, variant)
+
+
 def _check_w(W, N: int, K: int, variant: int):
     torch = _torch()
     if W.dtype != torch.uint8 or not W.is_cuda or not W.is_contiguous():
         raise TypeError("W must be a contiguous uint8 CUDA tensor")
-    if W.numel() < N * row_bytes(K, variant):
+    if W.numel() < N * _row_bytes_fast(K, variant):
         raise ValueError("W holds fewer than N * row_bytes bytes")
 
 
