@@ -471,17 +471,29 @@ def copies_for(mats, variant):
 
 def per_matrix_kernel_times(L: GemvStep, reps=None):
     """Average device time of each matrix's kernel: a CUDA graph of `reps` launches
-    of that matrix's product (rotating over the resident copies, so every launch
-    streams from HBM) is replayed between CUDA events on the launching stream."""
+    of that matrix's product is replayed between CUDA events on the launching
+    stream.  The launches rotate over copies of the matrix whose total exceeds
+    four times the L2 (the resident layer copies plus extra copies for small
+    matrices), so every launch streams its weights from HBM."""
     import torch
-    reps = reps or max(20, 2 * L.copies)
+
+    import synth
+    import synth.device
     out = []
     for m, (name, N, K) in enumerate(L.mats):
+        nbytes = N * L.rf4.row_bytes(K, L.variant)
+        ncopies = max(L.copies, int(np.ceil(4 * L2_BYTES / nbytes)) + 1)
+        Ws = [L.W[r][m] for r in range(L.copies)]
+        for r in range(L.copies, ncopies):
+            w = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            synth.device.fill_weights(w, N, K, L.variant, seed=1000 + r, stream=synth.weight_stream(0, m))
+            Ws.append(w)
+        n = reps or max(20, 2 * ncopies)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for i in range(reps):
-                r = i % L.copies
-                L.rf4.gemm(L.W[r][m], L.X[r][m], N, K, L.variant, Y=L.Y[r][m])
+            for i in range(n):
+                r = i % ncopies
+                L.rf4.gemm(Ws[r], L.X[r % L.copies][m], N, K, L.variant, Y=L.Y[r % L.copies][m])
         g.replay()
         torch.cuda.synchronize()
         s = torch.cuda.current_stream()
@@ -491,8 +503,9 @@ def per_matrix_kernel_times(L: GemvStep, reps=None):
             g.replay()
         e1.record(s)
         e1.synchronize()
-        out.append(e0.elapsed_time(e1) / 1e3 / (3 * reps))
-        del g
+        out.append(e0.elapsed_time(e1) / 1e3 / (3 * n))
+        del g, Ws
+    torch.cuda.empty_cache()
     return out
 
 
