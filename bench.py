@@ -469,12 +469,16 @@ def copies_for(mats, variant):
     return max(2, int(np.ceil(4 * L2_BYTES / weight_bytes(mats, variant))) + 1)
 
 
-def per_matrix_kernel_times(L: GemvStep, reps=None):
+def per_matrix_kernel_times(L: GemvStep, reps=None, ceilings=None):
     """Average device time of each matrix's kernel: a CUDA graph of `reps` launches
     of that matrix's product is replayed between CUDA events on the launching
     stream.  The launches rotate over copies of the matrix whose total exceeds
     four times the L2 (the resident layer copies plus extra copies for small
-    matrices), so every launch streams its weights from HBM."""
+    matrices), so every launch streams its weights from HBM.  If `ceilings` is
+    a list, it receives per matrix the device time of a plain read of the same
+    bytes by a library reduction (torch.sum over the blocks viewed as fp32),
+    in the same graph shape over the same copies: what one kernel of that size
+    reaches without any decode."""
     import torch
 
     import synth
@@ -504,7 +508,23 @@ def per_matrix_kernel_times(L: GemvStep, reps=None):
         e1.record(s)
         e1.synchronize()
         out.append(e0.elapsed_time(e1) / 1e3 / (3 * n))
-        del g, Ws
+        del g
+        if ceilings is not None and nbytes % 4 == 0:
+            sinks = torch.empty(n, dtype=torch.float32, device="cuda")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    torch.sum(Ws[i % ncopies].view(torch.float32), dim=0, out=sinks[i])
+            g.replay()
+            torch.cuda.synchronize()
+            e0.record(s)
+            for _ in range(3):
+                g.replay()
+            e1.record(s)
+            e1.synchronize()
+            ceilings.append(e0.elapsed_time(e1) / 1e3 / (3 * n))
+            del g, sinks
+        del Ws
     torch.cuda.empty_cache()
     return out
 
@@ -548,7 +568,8 @@ def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True):
         t = time_runs(L.run_steps, args.steps, args.warmup, world)
     t = max_over_ranks(t, world)
     sb = step_bytes(mats, variant, M)
-    kt = per_matrix_kernel_times(L)
+    ceil = []
+    kt = per_matrix_kernel_times(L, ceilings=ceil)
     algo = [matrix_bytes(N, K, variant) + 2 * M * K + 4 * M * N for _, N, K in mats]
     achieved = sum(algo) / sum(kt) / 1e9
     res = dict(
@@ -557,6 +578,9 @@ def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True):
         footprint_gb=round(copies * weight_bytes(mats, variant) / 1e9, 3),
         per_launch_us={n: round(x * 1e6, 2) for (n, _, _), x in zip(mats, kt)},
         achieved=achieved, algo_bytes={n: a for (n, _, _), a in zip(mats, algo)}, kernel_s=kt,
+        read_ceiling_us={n: round(x * 1e6, 2) for (n, _, _), x in zip(mats, ceil)} if len(ceil) == len(mats) else None,
+        read_ceiling_gbs={n: round(matrix_bytes(N, K, variant) / x / 1e9, 1) for (n, N, K), x in zip(mats, ceil)}
+        if len(ceil) == len(mats) else None,
         graph_launch_check=L.rf4.launch_count() - launches0)
     if with_e2e:
         ne = max(10, args.steps // 4)
@@ -986,6 +1010,11 @@ def gemv_roofline(res, hbm, peak_kind, mats, variant, M):
             "kernel": "gemv_stream_kernel", "peak_kind": peak_kind, "frac_of": f"{peak_kind} HBM copy bandwidth",
             "per_launch_us": res["per_launch_us"],
             "algorithmic_bytes_per_launch": res["algo_bytes"]}
+    if res.get("read_ceiling_us"):
+        roof["read_ceiling"] = {"us": res["read_ceiling_us"], "GB/s": res["read_ceiling_gbs"],
+                                "note": "a plain read of each matrix's bytes by one library kernel (torch.sum of the "
+                                        "blocks as fp32), same graph and copies: what one launch of that size reaches "
+                                        "without any decode"}
     if traffic and all(n in traffic for n, _, _ in mats):
         roof["traffic"] = int(round(sum(traffic[n] for n, _, _ in mats) / len(mats)))
         roof["traffic_per_launch"] = {n: traffic[n] for n, _, _ in mats}
