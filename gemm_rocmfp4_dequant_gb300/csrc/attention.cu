@@ -68,10 +68,9 @@ struct AttnFmt {
   static constexpr int STAGE = 2 * CB;              // K chunk then V chunk
   static constexpr int KS = D / 16;                 // MMA k steps over D
   static constexpr int WARP_RING = kAttnStages * STAGE;
-  static constexpr int PBUF = 8 * kChunk * 4;       // P[8 heads][32 tokens] fp32
   static constexpr int MERGE = partial_floats(D) * 4;  // one warp's state for the merge
-  // per warp: ring, then P buffer; the merge area reuses the rings
-  static constexpr int WARP_BYTES = WARP_RING + PBUF;
+  // per warp: its ring; the merge area reuses the rings
+  static constexpr int WARP_BYTES = WARP_RING;
   static constexpr int BAR_OFF = kAttnWarps * WARP_BYTES;
   static constexpr int SMEM = BAR_OFF + kAttnWarps * kAttnStages * 8;
   static_assert(kAttnWarps * MERGE <= kAttnWarps * WARP_RING, "merge area fits in the rings");
@@ -129,15 +128,17 @@ RF4_DEV void decode4(uint32_t codes, uint32_t s2, uint32_t (&v)[4]) {
   v[3] = hmul2(clamp5(e2m1x2<3>(codes)), s2);
 }
 
+// The MMA and movmatrix wrappers below touch registers only, so they are not
+// volatile: the compiler may schedule them among the softmax's dependent steps.
 RF4_DEV void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 RF4_DEV void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -147,8 +148,16 @@ RF4_DEV void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32
 // (r, c) holds elements (r, 2c) and (r, 2c+1)).
 RF4_DEV uint32_t movmatrix_t(uint32_t a) {
   uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = +0,
+// subnormal results flush to zero).
+RF4_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 RF4_DEV uint32_t pack_half2(float lo, float hi) {
@@ -157,6 +166,19 @@ RF4_DEV uint32_t pack_half2(float lo, float hi) {
 }
 
 // p = hi + lo in two fp16 pairs (p already scaled by 2^15).
+// C = 0 form of mma_f16 / mma_bf16.
+RF4_DEV void mma_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, bool bf16) {
+  const float z = 0.f;
+  if (bf16)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
 RF4_DEV void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(a, b);
   hi = *reinterpret_cast<const uint32_t*>(&h);
@@ -173,7 +195,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
   const int bhk = blockIdx.x / S, split = blockIdx.x % S;
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
   uint8_t* ring = smem + (size_t)warp * F::WARP_BYTES;
-  float* pbuf = reinterpret_cast<float*>(ring + F::WARP_RING);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + F::BAR_OFF) + warp * kAttnStages;
   if (lane == 0) {
     for (int i = 0; i < kAttnStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -208,6 +229,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
 
   // online softmax state of heads 2c and 2c+1 (base-2 scores), and P.V in
   // fragments: oacc[m] for D rows 16m .. 16m+15 (block m/2, half m%2)
+  // (lrun holds this lane's tokens only; the lanes' parts are added after the loop)
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
   float oacc[2 * F::NB][4];
 #pragma unroll
@@ -242,7 +264,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
     float sacc[2][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
       const uint32_t ra = ks_base + (uint32_t)(16 * mt + r) * F::RB, rb = ra + 8 * F::RB;
 #pragma unroll
       for (int kb = 0; kb < F::NB; ++kb) {
@@ -260,7 +281,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t a[4] = {va[2 * h], vb[2 * h], va[2 * h + 1], vb[2 * h + 1]};
-          if constexpr (ACT == 1)
+          if (kb == 0 && h == 0)  // the first step starts from zero
+            mma_z(sacc[mt], a, qb0[0], qb1[0], ACT == 1);
+          else if constexpr (ACT == 1)
             mma_bf16(sacc[mt], a, qb0[2 * kb + h], qb1[2 * kb + h]);
           else
             mma_f16(sacc[mt], a, qb0[2 * kb + h], qb1[2 * kb + h]);
@@ -269,60 +292,70 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
     }
 
     // ---- online softmax over the chunk (heads 2c, 2c+1 in this lane) ----
+    // Every chunk holds at least one token of the sequence, so each running
+    // max is finite from the first chunk on, and 2^(-inf - max) = 0 needs no
+    // guard.
     float x[2][4], cmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = t0 + 16 * mt + r + (e >= 2 ? 8 : 0);
-        const float v = tok < T ? sacc[mt][e] * p.scale_log2 : -INFINITY;
-        x[mt][e] = v;
-        cmax[e & 1] = fmaxf(cmax[e & 1], v);
-      }
+      for (int e = 0; e < 4; ++e) x[mt][e] = sacc[mt][e] * p.scale_log2;
+    if (t0 + kChunk > T) {  // only the last chunk has tokens past the sequence
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (t0 + 16 * mt + r + (e >= 2 ? 8 : 0) >= T) x[mt][e] = -INFINITY;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cmax[e & 1] = fmaxf(cmax[e & 1], x[mt][e]);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 4));
       cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 8));
       cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 16));
     }
-    float alpha[2], mnew[2], psum[2] = {0.f, 0.f};
+    float alpha[2], mnew[2], psum[2] = {0.f, 0.f}, pv[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       mnew[j] = fmaxf(mrun[j], cmax[j]);
-      alpha[j] = mnew[j] == -INFINITY ? 1.f : exp2f(mrun[j] - mnew[j]);
+      alpha[j] = ex2_approx(mrun[j] - mnew[j]);
     }
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = e & 1;
-        const float pv = mnew[j] == -INFINITY ? 0.f : exp2f(x[mt][e] - mnew[j]);
-        psum[j] += pv;
-        pbuf[(2 * c + j) * kChunk + 16 * mt + r + (e >= 2 ? 8 : 0)] = pv;
+        pv[mt][e] = ex2_approx(x[mt][e] - mnew[j]);
+        psum[j] += pv[mt][e];
       }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      psum[j] += __shfl_xor_sync(0xffffffffu, psum[j], 4);
-      psum[j] += __shfl_xor_sync(0xffffffffu, psum[j], 8);
-      psum[j] += __shfl_xor_sync(0xffffffffu, psum[j], 16);
       lrun[j] = lrun[j] * alpha[j] + psum[j];
       mrun[j] = mnew[j];
     }
-    __syncwarp();
 
-    // ---- P.V: k steps of 16 tokens (kk), A = V^T by movmatrix, B = P^T.
+    // ---- P.V: k steps of 16 tokens (kk), A = V^T by movmatrix, B = P^T (P's
+    // score fragments, split into fp16 pairs and transposed by movmatrix).
     // The chunk's products accumulate in fresh registers (4 MMAs deep), then
     // o = o * alpha + chunk in fp32 round to nearest.
     float cacc[2 * F::NB][4];
 #pragma unroll
-    for (int m = 0; m < 2 * F::NB; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
-#pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       uint32_t bh0, bl0, bh1, bl1;
       {
-        const float* pr = pbuf + r * kChunk + 16 * kk + 2 * c;  // head r, tokens 2c, 2c+1, 2c+8, 2c+9
-        split_half2(pr[0] * kPScale, pr[1] * kPScale, bh0, bl0);
-        split_half2(pr[8] * kPScale, pr[9] * kPScale, bh1, bl1);
+        // lane (r, c) holds P of token 16kk + r (+ 8) for heads 2c, 2c+1: an
+        // 8 x 8 (token, head) fragment; its transpose gives lane (r, c) head r
+        // at tokens 2c, 2c+1 (+ 8), the B fragment
+        uint32_t h0, l0, h1, l1;
+        split_half2(pv[kk][0] * kPScale, pv[kk][1] * kPScale, h0, l0);
+        split_half2(pv[kk][2] * kPScale, pv[kk][3] * kPScale, h1, l1);
+        bh0 = movmatrix_t(h0);
+        bl0 = movmatrix_t(l0);
+        bh1 = movmatrix_t(h1);
+        bl1 = movmatrix_t(l1);
       }
       const int ta = t0 + 16 * kk + r, tb = ta + 8;  // this lane's tokens in the movmatrix inputs
       const uint32_t ra = vs_base + (uint32_t)(16 * kk + r) * F::RB, rb = ra + 8 * F::RB;
@@ -343,7 +376,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
         for (int h = 0; h < 2; ++h) {
           const uint32_t a[4] = {movmatrix_t(va[2 * h]), movmatrix_t(va[2 * h + 1]), movmatrix_t(vb[2 * h]),
                                  movmatrix_t(vb[2 * h + 1])};
-          mma_f16(cacc[2 * kb + h], a, bh0, bh1);
+          if (kk == 0)  // the first step starts from zero
+            mma_z(cacc[2 * kb + h], a, bh0, bh1, false);
+          else
+            mma_f16(cacc[2 * kb + h], a, bh0, bh1);
           mma_f16(cacc[2 * kb + h], a, bl0, bl1);
         }
       }
@@ -365,6 +401,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
   if (!ok) {
     if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
     for (int k = 0; k < issued; ++k) (void)mbar_wait_bounded(smem_addr(&bars[k % kAttnStages]), (uint32_t)((k / kAttnStages) & 1));
+  }
+
+  // the running sums of the 8 lanes of each head pair (fixed order)
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    lrun[j] += __shfl_xor_sync(0xffffffffu, lrun[j], 4);
+    lrun[j] += __shfl_xor_sync(0xffffffffu, lrun[j], 8);
+    lrun[j] += __shfl_xor_sync(0xffffffffu, lrun[j], 16);
   }
 
   // ---- merge the warps' states (warp order), then output or split partial ----
