@@ -77,25 +77,25 @@ struct AttnFmt {
   static_assert(CB % 16 == 0, "bulk copies of whole chunks");
 };
 
-RF4_DEV uint32_t lds32(uint32_t saddr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
-  return v;
-}
+// Shared-memory loads are plain C++ loads, so the compiler may schedule them
+// early (the mbarrier wait and the proxy fence carry "memory" clobbers, which
+// keep them after the data lands and before the stage is refilled).
+RF4_DEV uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 // Four bytes at any shared-memory address (two aligned words and a funnel shift).
-RF4_DEV uint32_t lds_bytes4(uint32_t saddr) {
-  const uint32_t a = saddr & ~3u;
-  return __funnelshift_r(lds32(a), lds32(a + 4), (saddr & 3u) * 8u);
+RF4_DEV uint32_t lds_bytes4(const uint8_t* p) {
+  const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(p) & 3u;
+  const uint8_t* a = p - mis;
+  return __funnelshift_r(lds32(a), lds32(a + 4), mis * 8u);
 }
 
 // Four bytes at an address whose offset from a 4-byte boundary is al (0..3),
 // or not known (al = -1).  Called with al a constant after unrolling, so the
 // branches fold away.
-RF4_DEV uint32_t lds_bytes4_al(uint32_t saddr, int al) {
-  if (al == 0) return lds32(saddr);
-  if (al > 0) return __funnelshift_r(lds32(saddr - al), lds32(saddr - al + 4), 8 * al);
-  return lds_bytes4(saddr);
+RF4_DEV uint32_t lds_bytes4_al(const uint8_t* p, int al) {
+  if (al == 0) return lds32(p);
+  if (al > 0) return __funnelshift_r(lds32(p - al), lds32(p - al + 4), 8 * al);
+  return lds_bytes4(p);
 }
 
 // Offset from a 4-byte boundary of byte `off` of a token row, when rows start
@@ -109,9 +109,10 @@ RF4_HOSTDEV constexpr int row_align(int off) {
 // Scale pair of a block as f16x2 E4M3 values: (scale of weights 0-15, scale
 // of weights 16-31); the single-scale variant repeats its one scale.
 template <int V>
-RF4_DEV uint32_t block_scales(uint32_t block_saddr, int al) {
-  const uint32_t a = block_saddr + 16;
-  const uint32_t w = al >= 0 ? lds32(a - al) >> (8 * al) : lds32(a & ~3u) >> ((a & 3u) * 8u);
+RF4_DEV uint32_t block_scales(const uint8_t* block, int al) {
+  const uint8_t* a = block + 16;
+  const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(a) & 3u;
+  const uint32_t w = al >= 0 ? lds32(a - al) >> (8 * al) : lds32(a - mis) >> (mis * 8u);
   if constexpr (V == 0) {
     return e4m3x2<0>(w & 0xFFFFu);  // two bytes, never straddling a word (even address)
   } else {
@@ -256,15 +257,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
       ok = false;
       break;
     }
-    const uint32_t ks_base = smem_addr(ring + (size_t)st * F::STAGE);
-    const uint32_t vs_base = ks_base + F::CB;
+    const uint8_t* ks_base = ring + (size_t)st * F::STAGE;
+    const uint8_t* vs_base = ks_base + F::CB;
     const int t0 = ch * kChunk;  // first token of the chunk
 
     // ---- scores: token rows 16mt + r and 16mt + r + 8 ----
     float sacc[2][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      const uint32_t ra = ks_base + (uint32_t)(16 * mt + r) * F::RB, rb = ra + 8 * F::RB;
+      const uint8_t* ra = ks_base + (16 * mt + r) * F::RB;
+      const uint8_t* rb = ra + 8 * F::RB;
 #pragma unroll
       for (int kb = 0; kb < F::NB; ++kb) {
         uint32_t va[4], vb[4];
@@ -358,7 +360,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const __gri
         bl1 = movmatrix_t(l1);
       }
       const int ta = t0 + 16 * kk + r, tb = ta + 8;  // this lane's tokens in the movmatrix inputs
-      const uint32_t ra = vs_base + (uint32_t)(16 * kk + r) * F::RB, rb = ra + 8 * F::RB;
+      const uint8_t* ra = vs_base + (16 * kk + r) * F::RB;
+      const uint8_t* rb = ra + 8 * F::RB;
 #pragma unroll
       for (int kb = 0; kb < F::NB; ++kb) {
         uint32_t va[4], vb[4];
