@@ -476,13 +476,15 @@ def per_matrix_kernel_times(L: GemvStep, reps=None, ceilings=None):
     four times the L2 (the resident layer copies plus extra copies for small
     matrices), so every launch streams its weights from HBM.  If `ceilings` is
     a list, it receives per matrix the device time of a plain read of the same
-    bytes by a library reduction (torch.sum over the blocks viewed as fp32),
-    in the same graph shape over the same copies: what one kernel of that size
-    reaches without any decode."""
+    bytes (ceiling/read.cu: bulk copies into shared memory and an XOR checksum
+    of every word, no decode), in the same graph shape over the same copies,
+    the fastest of ceiling.CONFIGS: what one launch of that size reaches
+    without any decode or arithmetic."""
     import torch
 
     import synth
     import synth.device
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     out = []
     for m, (name, N, K) in enumerate(L.mats):
         nbytes = N * L.rf4.row_bytes(K, L.variant)
@@ -509,21 +511,29 @@ def per_matrix_kernel_times(L: GemvStep, reps=None, ceilings=None):
         e1.synchronize()
         out.append(e0.elapsed_time(e1) / 1e3 / (3 * n))
         del g
-        if ceilings is not None and nbytes % 4 == 0:
-            sinks = torch.empty(n, dtype=torch.float32, device="cuda")
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for i in range(n):
-                    torch.sum(Ws[i % ncopies].view(torch.float32), dim=0, out=sinks[i])
-            g.replay()
-            torch.cuda.synchronize()
-            e0.record(s)
-            for _ in range(3):
+        if ceilings is not None and nbytes % 16 == 0:
+            import ceiling
+            sink = torch.zeros(2, dtype=torch.int32, device="cuda")
+            best = None
+            for cfg in ceiling.CONFIGS:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(n):
+                        ceiling.read(Ws[i % ncopies], sink, cfg, sms)
                 g.replay()
-            e1.record(s)
-            e1.synchronize()
-            ceilings.append(e0.elapsed_time(e1) / 1e3 / (3 * n))
-            del g, sinks
+                torch.cuda.synchronize()
+                e0.record(s)
+                for _ in range(3):
+                    g.replay()
+                e1.record(s)
+                e1.synchronize()
+                t = e0.elapsed_time(e1) / 1e3 / (3 * n)
+                best = t if best is None or t < best else best
+                del g
+            if int(sink[1].item()) != 0:
+                raise RuntimeError("read ceiling kernel: a bounded wait gave up")
+            ceilings.append(best)
+            del sink
         del Ws
     torch.cuda.empty_cache()
     return out
@@ -1012,9 +1022,9 @@ def gemv_roofline(res, hbm, peak_kind, mats, variant, M):
             "algorithmic_bytes_per_launch": res["algo_bytes"]}
     if res.get("read_ceiling_us"):
         roof["read_ceiling"] = {"us": res["read_ceiling_us"], "GB/s": res["read_ceiling_gbs"],
-                                "note": "a plain read of each matrix's bytes by one library kernel (torch.sum of the "
-                                        "blocks as fp32), same graph and copies: what one launch of that size reaches "
-                                        "without any decode"}
+                                "note": "a plain read of each matrix's bytes (ceiling/read.cu: bulk copies into shared "
+                                        "memory, XOR checksum of every word; fastest of four grid shapes), same graph "
+                                        "and copies: what one launch of that size reaches without decode or arithmetic"}
     if traffic and all(n in traffic for n, _, _ in mats):
         roof["traffic"] = int(round(sum(traffic[n] for n, _, _ in mats) / len(mats)))
         roof["traffic_per_launch"] = {n: traffic[n] for n, _, _ in mats}

@@ -146,3 +146,19 @@ def test_layer_passes_replay_whole_rotations_and_count_exactly():
                 for tag in log:
                     passes.extend(range(copies) if tag == "multi" else [tag])
                 assert passes == [(first + i) % copies for i in range(n)], (copies, first, n, log)
+
+
+def test_read_ceiling_kernel_builds_and_exports():
+    # the benchmark's plain-read ceiling kernel: a separate measurement library
+    import ctypes
+
+    import ceiling
+    L = ctypes.CDLL(ceiling.build())
+    for sym in ("readceil_launch", "readceil_prepare", "readceil_smem"):
+        assert hasattr(L, sym), sym
+    L.readceil_smem.restype = ctypes.c_size_t
+    for chunk, warps, per_sm, stages in ceiling.CONFIGS:
+        smem = L.readceil_smem(chunk, warps, stages)
+        assert smem == warps * stages * (chunk + 8)
+        assert smem * per_sm <= 228 * 1024 and smem <= ceiling.MAX_SMEM  # the CTAs of a config fit on an SM
+        assert chunk % 512 == 0
