@@ -494,7 +494,7 @@ def per_matrix_kernel_times(L: GemvStep, reps=None, ceilings=None):
             w = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
             synth.device.fill_weights(w, N, K, L.variant, seed=1000 + r, stream=synth.weight_stream(0, m))
             Ws.append(w)
-        n = reps or max(20, 2 * ncopies)
+        n = reps or max(50, 2 * ncopies)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(n):
