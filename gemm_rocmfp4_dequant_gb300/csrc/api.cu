@@ -21,7 +21,6 @@ struct DeviceState {
   float* ws = nullptr;               // 2 * wmax records of kStreamTileRows * 8 floats
   uint32_t* cnt = nullptr;           // wmax split counters
   uint32_t* err = nullptr;           // kernel error bits
-  uint32_t* gbar = nullptr;          // grid barrier counter of chained launches
   float* tcws = nullptr;             // tensor-core kernel: split-tile partials
   uint32_t* tccnt = nullptr;         // tensor-core kernel: split-tile counters
   float* attn_ws = nullptr;          // decode attention: split partials
@@ -79,8 +78,6 @@ rocmfp4_status device_state(DeviceState** out) {
     if ((e = cudaMalloc(&d.ws, sizeof(float) * kStreamTileRows * 8 * 2 * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.cnt, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMalloc(&d.err, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
-    if ((e = cudaMalloc(&d.gbar, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
-    if ((e = cudaMemset(d.gbar, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaMalloc(&d.vfirst, sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(d.cnt, 0, sizeof(uint32_t) * d.wmax)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
     if ((e = cudaMalloc(&d.tcws, sizeof(float) * tc_ws_floats(d.sms))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
@@ -215,33 +212,6 @@ rocmfp4_status product(const void* W, const void* X, float* Y, int64_t M, int64_
   return ROCMFP4_OK;
 }
 
-// Arguments of the streaming kernel for one product (M <= 8, stream-eligible).
-GemvArgs stream_args(const DeviceState* d, const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
-                     int variant, int64_t wact) {
-  const int64_t ku = stream_weights_per_unit(variant);
-  GemvArgs a{};
-  a.W = static_cast<const uint8_t*>(W);
-  a.X = static_cast<const uint16_t*>(X);
-  a.Y = Y;
-  a.N = N;
-  a.K = K;
-  a.row_bytes = K / 32 * block_bytes_of(variant);
-  a.M = (int)M;
-  a.nspans = K / ku;
-  a.units = (N + kStreamTileRows - 1) / kStreamTileRows * a.nspans;
-  a.wact = wact;
-  a.ws = d->ws;
-  a.cnt = d->cnt;
-  a.err = d->err;
-  return a;
-}
-
-bool chain_eligible(const rocmfp4_gemv_op& op, int64_t M, int variant) {
-  const int64_t ku = stream_weights_per_unit(variant);
-  return M >= 1 && M <= 8 && op.N > 0 && op.K > 0 && op.K % ku == 0 && aligned16(op.W) && aligned16(op.X) &&
-         (op.N + kStreamTileRows - 1) / kStreamTileRows * (op.K / ku) < (int64_t(1) << 31);
-}
-
 rocmfp4_status chain(const rocmfp4_gemv_op* ops, int count, int64_t M, int variant, int act, cudaStream_t s) {
   if (count < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative count");
   if (count == 0) return ROCMFP4_OK;
@@ -257,44 +227,16 @@ rocmfp4_status chain(const rocmfp4_gemv_op* ops, int count, int64_t M, int varia
       return fail(ROCMFP4_ERR_INVALID_ARG, "product " + std::to_string(i) + ": NULL pointer");
   }
   if (M == 0) return ROCMFP4_OK;
-  DeviceState* d = nullptr;
-  rocmfp4_status st = device_state(&d);
-  if (st != ROCMFP4_OK) return st;
-  const int mb = stream_mb_for((int)(M < 8 ? M : 8));
-  const int lm = mb == 1 ? 0 : mb == 2 ? 1 : mb == 4 ? 2 : 3;
-  const int64_t cap = (int64_t)d->sms * d->occ[variant][act][lm] * kStreamWarpsPerCta;
-  int i = 0;
-  while (i < count) {
-    if (ops[i].N == 0) {
-      ++i;
-      continue;
-    }
-    if (!chain_eligible(ops[i], M, variant)) {
-      st = product(ops[i].W, ops[i].X, ops[i].Y, M, ops[i].N, ops[i].K, variant, act, s);
-      if (st != ROCMFP4_OK) return st;
-      ++i;
-      continue;
-    }
-    // a run of eligible products, at most kChainOps; each product's units go
-    // to the warps a single call would give them, so the sums are the same
-    int n = 0;
-    int64_t wmax = 0;
-    GemvArgs args[kChainOps];
-    while (i + n < count && n < kChainOps && ops[i + n].N > 0 && chain_eligible(ops[i + n], M, variant)) {
-      const rocmfp4_gemv_op& op = ops[i + n];
-      const int64_t ku = stream_weights_per_unit(variant);
-      const int64_t w =
-          stream_warps((op.N + kStreamTileRows - 1) / kStreamTileRows, op.K / ku, ku * block_bytes_of(variant), M, cap);
-      args[n] = stream_args(d, op.W, op.X, op.Y, M, op.N, op.K, variant, w);
-      wmax = w > wmax ? w : wmax;
-      ++n;
-    }
-    const int ctas = (int)((wmax + kStreamWarpsPerCta - 1) / kStreamWarpsPerCta);
-    cudaError_t e = n == 1 ? launch_gemv_stream(variant, act, args[0], ctas, s)
-                           : launch_gemv_chain(variant, act, args, n, d->gbar, ctas, s);
-    if (e != cudaSuccess) return cuda_fail(e, n == 1 ? "streaming kernel launch" : "chained streaming launch");
-    g_launches.fetch_add(1);
-    i += n;
+  // One launch per product, in order, exactly as rocmfp4_gemm_ex would run
+  // it.  Streaming launches are programmatic dependent launches: a product's
+  // weights stream while the previous product finishes, and its activations
+  // are read only once the previous launch has completed.  (One cooperative
+  // launch with a grid barrier between products measured slower at every
+  // size, from N = 256 to the layer's matrices.)
+  for (int i = 0; i < count; ++i) {
+    if (ops[i].N == 0) continue;
+    rocmfp4_status st = product(ops[i].W, ops[i].X, ops[i].Y, M, ops[i].N, ops[i].K, variant, act, s);
+    if (st != ROCMFP4_OK) return st;
   }
   return ROCMFP4_OK;
 }
@@ -539,7 +481,6 @@ uint32_t rocmfp4_device_error_bits(rocmfp4_stream_t stream) {
       // A kernel gave up waiting: its split counters may be left set, so clear them.
       cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s);
       cudaMemsetAsync(d->cnt, 0, sizeof(uint32_t) * d->wmax, s);
-      cudaMemsetAsync(d->gbar, 0, sizeof(uint32_t), s);
       cudaMemsetAsync(d->tccnt, 0, sizeof(uint32_t) * tc_cnt_words(d->sms), s);
       if (cudaStreamSynchronize(s) != cudaSuccess) return 0xFFFFFFFFu;
     }
@@ -577,7 +518,6 @@ void rocmfp4_shutdown(void) {
     cudaFree(d.ws);
     cudaFree(d.cnt);
     cudaFree(d.err);
-    cudaFree(d.gbar);
     cudaFree(d.tcws);
     cudaFree(d.tccnt);
     cudaFree(d.attn_ws);

@@ -82,7 +82,7 @@ constexpr int kZeroBytes = 256;  // zero activations for lanes whose B column is
 template <int V, int MB, int DEEP = 0>
 constexpr size_t smem_bytes() {
   return (size_t)kWarps * stages<V, MB, DEEP>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB, DEEP>() * 8 +
-         16 + cta_red_bytes<MB>() + kZeroBytes;
+         cta_red_bytes<MB>() + kZeroBytes;
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -173,112 +173,14 @@ struct StreamOp {
   int64_t wact;  // warps sharing this product's units (<= units and <= the launch's warps)
 };
 
-// Parameters of a launch over NOPS products (NOPS = 1: a single product).
-template <int NOPS>
+// Parameters of a launch.
 struct StreamParams {
-  StreamOp op[NOPS];
+  StreamOp op;
   float* ws;       // 2 * wact records of 32 x 8 floats
   uint32_t* cnt;   // split-tile counters, zero between launches
   uint32_t* err;   // error bits
-  uint32_t* gbar;  // grid barrier counter of a chain, zero between launches
-  int64_t wact;    // warps of the launch
-  int nops;
   int M;
 };
-
-// A warp's position in its sequence of units across the products of a
-// launch: product g, the k-th of its n units of that product, and the unit's
-// (tile, span).
-struct Cursor {
-  int g, k, n, t, j;
-};
-
-// Moves the cursor to the first unit of the first product >= g in which the
-// warp owns units (g = nops when there is none).
-template <int NOPS>
-RF4_DEV void cursor_begin(Cursor& c, const StreamParams<NOPS>& p, int g, int64_t wg) {
-  for (; g < p.nops; ++g) {
-    const int64_t U = p.op[g].units, W = p.op[g].wact;
-    if (wg >= W) continue;
-    const int64_t u0 = U * wg / W, u1 = U * (wg + 1) / W;
-    if (u1 > u0) {
-      c.g = g;
-      c.k = 0;
-      c.n = (int)(u1 - u0);
-      c.t = (int)(u0 / p.op[g].nspans);
-      c.j = (int)(u0 % p.op[g].nspans);
-      return;
-    }
-  }
-  c.g = p.nops;
-  c.k = c.n = c.t = c.j = 0;
-}
-
-template <int NOPS>
-RF4_DEV void cursor_next(Cursor& c, const StreamParams<NOPS>& p, int64_t wg) {
-  if (++c.j == (int)p.op[c.g].nspans) {
-    c.j = 0;
-    ++c.t;
-  }
-  if (++c.k == c.n) cursor_begin(c, p, c.g + 1, wg);
-}
-
-// Grid-wide barrier number `gen` (1, 2, ...) of a chain.  The active warps
-// of a CTA meet on a shared-memory counter; the last of them arrives for the
-// CTA on the global counter (release: the CTA's stores of the previous
-// product, ordered before it by __syncwarp and the shared-memory
-// acquire/release chain, are published) and polls it, with back-off, until
-// all `ctas` CTAs have arrived `gen` times; the other warps poll the CTA's
-// shared-memory generation word.  Every wait gives up when a warp has
-// recorded an error or after about 2^32 cycles.
-RF4_DEV bool grid_barrier(uint32_t* gbar, uint32_t gen, uint32_t ctas, uint32_t warps_here, uint32_t* cta_count,
-                          uint32_t* cta_gen, uint32_t* err, int lane) {
-  __syncwarp();
-  int ok = 1;
-  if (lane == 0) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_addr(cta_count)) : "memory");
-    const long long t0 = clock64();
-    if (old + 1 == gen * warps_here) {
-      // last warp of the CTA: arrive on the grid counter and wait for everyone
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
-      uint32_t ns = 32;
-      while (true) {
-        uint32_t v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gbar) : "memory");
-        if (v >= gen * ctas) break;
-        if ((*reinterpret_cast<volatile uint32_t*>(err) & kErrWaitTimeout) || clock64() - t0 > (1ll << 32)) {
-          ok = 0;
-          break;
-        }
-        __nanosleep(ns);
-        ns = ns < 256 ? ns * 2 : 256;
-      }
-      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(cta_gen)), "r"(ok ? gen : 0xFFFFFFFFu)
-                   : "memory");
-    } else {
-      while (true) {
-        uint32_t v;
-        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(cta_gen)) : "memory");
-        if (v == 0xFFFFFFFFu) {
-          ok = 0;
-          break;
-        }
-        if (v >= gen) break;
-        if (clock64() - t0 > (1ll << 32)) {
-          ok = 0;
-          break;
-        }
-        __nanosleep(32);
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  // Activations written by other SMs are read next through the async proxy.
-  asm volatile("fence.proxy.async;" ::: "memory");
-  __syncwarp();
-  return ok != 0;
-}
 
 // Adds one unit's products into acc (see the kernel comment for the layouts).
 // Lanes whose B column carries no activations read theirs from `zero`, a
@@ -560,8 +462,8 @@ RF4_DEV uint32_t shared_add_acq_rel(uint32_t* p, uint32_t v) {
 // End of tile t of product op for this warp (its spans [js, j] are in acc):
 // store the tile if the warp covered all of it, else hand its partial to the
 // split-tile reduction.  Resets acc.
-template <int MB, int EPI, int NOPS>
-RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_t wg, int t, int js, int j, int lane,
+template <int MB, int EPI>
+RF4_DEV void finish_tile(const StreamParams& p, const StreamOp& op, int64_t wg, int t, int js, int j, int lane,
                          float (&acc)[2][4], const CtaRed& red) {
   constexpr bool COL = MB == 1;
   constexpr bool LOCAL = cta_red_bytes<MB>() > 0;  // level 1 in shared memory
@@ -673,281 +575,150 @@ RF4_DEV void finish_tile(const StreamParams<NOPS>& p, const StreamOp& op, int64_
     for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
 }
 
-// The streaming kernel over the NOPS products of a launch.  Each warp owns an
-// equal contiguous range of every product's units and streams them, product
-// after product, through its ring.  Weights never depend on earlier work, so
-// a warp keeps its ring full across product boundaries; a unit's activations
-// are copied only once everything it may depend on is complete: for the
-// first product, the preceding grid (programmatic dependent launch); for
-// product g > 0 of a chain, all warps' work on product g - 1 (grid barrier).
-// The barrier also makes the split-tile workspace free for the next product.
-// EPI = 1: the gate/up mode (single-product launches only).
-template <int V, int ACT, int MB, int NOPS, int EPI, int DEEP>
-__global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __grid_constant__ StreamParams<NOPS> p) {
+// The streaming kernel of one product.  Each warp owns an equal contiguous
+// range of the product's units (tile-major) and streams them through its
+// ring.  Weights never depend on earlier work: up to NS - 1 units of them are
+// requested before the programmatic-dependent-launch wait, so they stream
+// while the preceding grid drains; activations, outputs and the split-tile
+// workspace are touched only after the wait.
+// EPI = 1: the gate/up mode.
+template <int V, int ACT, int MB, int EPI, int DEEP>
+__global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __grid_constant__ StreamParams p) {
   using F = Fmt<V>;
   constexpr int NS = stages<V, MB, DEEP>();
   constexpr int SB = stage_bytes<V, MB>();
   extern __shared__ __align__(128) uint8_t smem[];
 
+  const StreamOp& op = p.op;
   const int M = p.M;
-  const int64_t wact = p.wact;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;
 
   uint8_t* ring = smem + (size_t)warp * NS * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * SB) + warp * NS;
-  // chain barrier words of the CTA (after every warp's stage barriers), then
-  // the shared part of the split-tile reduction
-  uint32_t* cta_count = reinterpret_cast<uint32_t*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
-  uint32_t* cta_gen = cta_count + 1;
+  // after every warp's stage barriers: the shared part of the split-tile
+  // reduction, then a page of zeros
   CtaRed red;
-  red.rec = reinterpret_cast<float*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + 16);
+  red.rec = reinterpret_cast<float*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
   red.cnt = reinterpret_cast<uint32_t*>(red.rec + kWarps * 2 * kTileRows * MB);  // used only if cta_red_bytes<MB>() > 0
-  uint4* zero = reinterpret_cast<uint4*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + 16 +
-                                         cta_red_bytes<MB>());
+  uint4* zero = reinterpret_cast<uint4*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + cta_red_bytes<MB>());
   if (threadIdx.x < kZeroBytes / 16) zero[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
-  const int64_t cta_first = (int64_t)blockIdx.x * kWarps;
-  const uint32_t warps_here = (uint32_t)(wact - cta_first < kWarps ? wact - cta_first : kWarps);
-  const uint32_t ctas = (uint32_t)((wact + kWarps - 1) / kWarps);
-  if (threadIdx.x == 0) {
-    *cta_count = 0u;
-    *cta_gen = 0u;
-  }
   if (cta_red_bytes<MB>() > 0 && threadIdx.x < kWarps) red.cnt[threadIdx.x] = 0u;
   __syncthreads();  // every thread of the CTA gets here: inactive warps return below
-  if (wg >= wact) return;
+  if (wg >= op.wact) return;
   if (lane == 0) {
-    for (int g = 0; g < p.nops && g < 4; ++g)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.op[g].tmw)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&op.tmw)) : "memory");
     for (int i = 0; i < NS; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  if constexpr (NOPS == 1) {
-    // A single product: this warp's units u0 .. u1 - 1, tile-major.  Weights
-    // of up to NS - 1 units are requested before the dependency wait; after
-    // it, each unit's activations go out with (or right after) its weights.
-    const StreamOp& op = p.op[0];
-    const int S = (int)op.nspans;
-    const int64_t u0 = op.units * wg / wact, u1 = op.units * (wg + 1) / wact;
-    const int n = (int)(u1 - u0);
-    int tw = (int)(u0 / S), jw = (int)(u0 % S), jx = jw;
-    int iw = 0, ix = 0, sw = 0, sx = 0;  // units issued (weights, activations) and their stages
-    auto issue_w1 = [&]() {
-      issue_w<V, MB, EPI>(&op.tmw, M, tw, jw, ring + (size_t)sw * SB, smem_addr(&bars[sw]), lane);
-      if (++jw == S) {
-        jw = 0;
-        ++tw;
-      }
-      if (++sw == NS) sw = 0;
-      ++iw;
-    };
-    auto issue_x1 = [&]() {
-      issue_x<V, MB>(op.X, op.K, M, jx, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
-      if (++jx == S) jx = 0;
-      if (++sx == NS) sx = 0;
-      ++ix;
-    };
-    while (iw < NS - 1 && iw < n) issue_w1();
-    grid_dependency_wait();
-    grid_launch_dependents();
-    __syncwarp();
-    while (ix < iw) issue_x1();
-
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    int t = (int)(u0 / S), j = (int)(u0 % S), js = j;
-    int k = 0, st = 0;
-    uint32_t phase = 0;
-    bool failed = false;
-    for (; k < n; ++k) {
-      if (iw < n) {  // unit k + NS - 1 goes into the stage unit k - 1 has released
-        issue_w1();
-        issue_x1();
-      }
-      if (!mbar_wait_bounded(smem_addr(&bars[st]), phase)) {
-        failed = true;
-        break;
-      }
-      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
-      __syncwarp();
-      fence_proxy_async();
-      if (j == S - 1 || k == n - 1) {
-        finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
-        js = 0;
-      }
-      if (++j == S) {
-        j = 0;
-        ++t;
-      }
-      if (++st == NS) {
-        st = 0;
-        phase ^= 1u;
-      }
+  // A single product: this warp's units u0 .. u1 - 1, tile-major.  Weights
+  // of up to NS - 1 units are requested before the dependency wait; after
+  // it, each unit's activations go out with (or right after) its weights.
+  const int S = (int)op.nspans;
+  const int64_t u0 = op.units * wg / op.wact, u1 = op.units * (wg + 1) / op.wact;
+  const int n = (int)(u1 - u0);
+  int tw = (int)(u0 / S), jw = (int)(u0 % S), jx = jw;
+  int iw = 0, ix = 0, sw = 0, sx = 0;  // units issued (weights, activations) and their stages
+  auto issue_w1 = [&]() {
+    issue_w<V, MB, EPI>(&op.tmw, M, tw, jw, ring + (size_t)sw * SB, smem_addr(&bars[sw]), lane);
+    if (++jw == S) {
+      jw = 0;
+      ++tw;
     }
-    if (failed) {
-      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      // every armed stage has its activation copies issued (ix == iw); let all copies land
-      for (; k < iw; ++k) {
-        (void)mbar_wait_bounded(smem_addr(&bars[st]), phase);
-        if (++st == NS) {
-          st = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    return;
-  }
-
-  // A chain.  cw: next unit whose weights to copy (the iw-th of this warp,
-  // into stage sw); cx: next unit whose activations to copy (ix <= iw, stage
-  // sx); activations of product g may be read once g <= readable.  Weights
-  // never depend on earlier work, so the ring stays full across products.
-  Cursor cw, cx;
-  cursor_begin(cw, p, 0, wg);
-  cx = cw;
-  int iw = 0, ix = 0, sw = 0, sx = 0, readable = 0;
-  auto issue_w_next = [&]() {
-    issue_w<V, MB, EPI>(&p.op[cw.g].tmw, M, cw.t, cw.j, ring + (size_t)sw * SB, smem_addr(&bars[sw]), lane);
-    const int g0 = cw.g;
-    ++iw;
     if (++sw == NS) sw = 0;
-    cursor_next(cw, p, wg);
-    if (cw.g != g0 && cw.g < p.nops && lane == 0)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.op[cw.g].tmw)) : "memory");
+    ++iw;
   };
-  auto issue_x_next = [&]() {
-    issue_x<V, MB>(p.op[cx.g].X, p.op[cx.g].K, M, cx.j, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
-    ++ix;
+  auto issue_x1 = [&]() {
+    issue_x<V, MB>(op.X, op.K, M, jx, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
+    if (++jx == S) jx = 0;
     if (++sx == NS) sx = 0;
-    cursor_next(cx, p, wg);
+    ++ix;
   };
-
-  // Start streaming weights, then wait for the preceding grid before
-  // touching activations, outputs or the split-reduction workspace.
-  while (iw < NS - 1 && cw.g < p.nops) issue_w_next();
+  while (iw < NS - 1 && iw < n) issue_w1();
   grid_dependency_wait();
   grid_launch_dependents();
   __syncwarp();
-  while (ix < iw && cx.g <= readable) issue_x_next();
+  while (ix < iw) issue_x1();
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  int i = 0, st = 0;  // this warp's unit being computed, its stage and the stage's phase
+  int t = (int)(u0 / S), j = (int)(u0 % S), js = j;
+  int k = 0, st = 0;
   uint32_t phase = 0;
   bool failed = false;
-  for (int g = 0; g < p.nops && !failed; ++g) {
-    if (g > 0) {
-      // fill the whole ring with weights of the products ahead, then wait
-      while (iw < i + NS && cw.g < p.nops) issue_w_next();
-      if (!grid_barrier(p.gbar, (uint32_t)g, ctas, warps_here, cta_count, cta_gen, p.err, lane)) {
-        failed = true;
-        break;
-      }
-      readable = g;
-      while (ix < iw && cx.g <= readable) issue_x_next();
+  for (; k < n; ++k) {
+    if (iw < n) {  // unit k + NS - 1 goes into the stage unit k - 1 has released
+      issue_w1();
+      issue_x1();
     }
-    const StreamOp& op = p.op[g];
-    if (wg >= op.wact) continue;
-    const int64_t U = op.units;
-    const int S = (int)op.nspans;
-    const int64_t u0 = U * wg / op.wact, u1 = U * (wg + 1) / op.wact;
-    const int nunits = (int)(u1 - u0);
-    int t = (int)(u0 / S), j = (int)(u0 % S), js = j;
-    for (int k = 0; k < nunits; ++k, ++i) {
-      // keep NS units in flight, counting the one being computed; a unit's
-      // activations follow its weights once its product is readable
-      if (iw < i + NS && cw.g < p.nops) issue_w_next();
-      if (ix < iw && cx.g <= readable) issue_x_next();
-      if (!mbar_wait_bounded(smem_addr(&bars[st]), phase)) {
-        failed = true;
-        break;
-      }
-      compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
-      __syncwarp();
-      fence_proxy_async();
-      if (j == S - 1 || k == nunits - 1) {
-        finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
-        js = 0;
-      }
-      if (++j == S) {
-        j = 0;
-        ++t;
-      }
-      if (++st == NS) {
-        st = 0;
-        phase ^= 1u;
-      }
+    if (!mbar_wait_bounded(smem_addr(&bars[st]), phase)) {
+      failed = true;
+      break;
+    }
+    compute_unit<V, ACT, MB>(ring + (size_t)st * SB, lane, M, acc, zero);
+    __syncwarp();
+    fence_proxy_async();
+    if (j == S - 1 || k == n - 1) {
+      finish_tile<MB, EPI>(p, op, wg, t, js, j, lane, acc, red);
+      js = 0;
+    }
+    if (++j == S) {
+      j = 0;
+      ++t;
+    }
+    if (++st == NS) {
+      st = 0;
+      phase ^= 1u;
     }
   }
-
   if (failed) {
     if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-    // Complete every armed stage (its activation copies too, whatever they
-    // read) and let all copies land before the shared memory is released.
-    readable = p.nops;
-    __syncwarp();
-    while (ix < iw) issue_x_next();
-    for (; i < iw; ++i) {
+    // every armed stage has its activation copies issued (ix == iw); let all copies land
+    for (; k < iw; ++k) {
       (void)mbar_wait_bounded(smem_addr(&bars[st]), phase);
       if (++st == NS) {
         st = 0;
         phase ^= 1u;
       }
     }
-  } else if (p.nops > 1) {
-    // Exit arrival: the CTA's last warp arrives once more on the grid counter
-    // (every CTA arrives nops times in all); the final arrival of the grid
-    // puts the counter back to zero for the next launch.
-    __syncwarp();
-    if (lane == 0) {
-      uint32_t old;
-      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_addr(cta_count)) : "memory");
-      if (old + 1 == (uint32_t)p.nops * warps_here) {
-        const uint32_t g_old = atomicAdd(p.gbar, 1u);
-        if (g_old + 1 == (uint32_t)p.nops * ctas) store_relaxed_gpu(p.gbar, 0u);
-      }
-    }
   }
 }
 
 // Kernel instance for (variant, activation type, staged activation rows,
-// single product or chain, plain or gate/up).
-template <int V, int ACT, int NOPS, int EPI>
+// plain or gate/up).
+template <int V, int ACT, int EPI>
 const void* kernel_for_mb(int mb) {
   switch (mb) {
-    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, NOPS, EPI, 0>);
-    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, NOPS, EPI, 0>);
-    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, NOPS, EPI, 0>);
-    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, NOPS, EPI, 0>);
+    case 1: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, EPI, 0>);
+    case 2: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, EPI, 0>);
+    case 4: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 4, EPI, 0>);
+    default: return reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 8, EPI, 0>);
   }
 }
 
-// The deep-ring instance of a single plain product (MB = 1 or 2 only).
+// The deep-ring instance of a plain product (MB = 1 or 2 only).
 template <int V, int ACT>
 const void* deep_kernel_for_mb(int mb) {
-  return mb == 1 ? reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, 1, 0, 1>)
-                 : reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, 1, 0, 1>);
+  return mb == 1 ? reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 1, 0, 1>)
+                 : reinterpret_cast<const void*>(&gemv_stream_kernel<V, ACT, 2, 0, 1>);
 }
 
 template <int EPI>
-const void* single_kernel(int variant, int act, int mb) {
-  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, 1, EPI>(mb) : kernel_for_mb<0, 1, 1, EPI>(mb);
-  return act == 0 ? kernel_for_mb<1, 0, 1, EPI>(mb) : kernel_for_mb<1, 1, 1, EPI>(mb);
+const void* plain_kernel(int variant, int act, int mb) {
+  if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, EPI>(mb) : kernel_for_mb<0, 1, EPI>(mb);
+  return act == 0 ? kernel_for_mb<1, 0, EPI>(mb) : kernel_for_mb<1, 1, EPI>(mb);
 }
 
-// kind 0: single product, 1: chain, 2: single gate/up product, 3: single
-// product with the deep ring (MB <= 2).
+// kind 0: plain product, 1: gate/up product, 2: plain product with the deep
+// ring (MB <= 2).
 const void* stream_kernel(int variant, int act, int mb, int kind) {
-  if (kind == 3) {
+  if (kind == 2) {
     if (variant == 0) return act == 0 ? deep_kernel_for_mb<0, 0>(mb) : deep_kernel_for_mb<0, 1>(mb);
     return act == 0 ? deep_kernel_for_mb<1, 0>(mb) : deep_kernel_for_mb<1, 1>(mb);
   }
-  if (kind == 1) {
-    if (variant == 0) return act == 0 ? kernel_for_mb<0, 0, kChainOps, 0>(mb) : kernel_for_mb<0, 1, kChainOps, 0>(mb);
-    return act == 0 ? kernel_for_mb<1, 0, kChainOps, 0>(mb) : kernel_for_mb<1, 1, kChainOps, 0>(mb);
-  }
-  return kind == 2 ? single_kernel<1>(variant, act, mb) : single_kernel<0>(variant, act, mb);
+  return kind == 1 ? plain_kernel<1>(variant, act, mb) : plain_kernel<0>(variant, act, mb);
 }
 
 template <int V>
@@ -971,27 +742,20 @@ size_t stream_smem_bytes(int variant, int mb, int deep) {
 }
 
 cudaError_t stream_prepare(int variant, int act, int mb) {
-  for (int kind = 0; kind < 4; ++kind) {
-    if (kind == 3 && mb > 2) break;
+  for (int kind = 0; kind < 3; ++kind) {
+    if (kind == 2 && mb > 2) break;
     cudaError_t e =
         cudaFuncSetAttribute(stream_kernel(variant, act, mb, kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem_bytes(variant, mb, kind == 3 ? 1 : 0));
+                             (int)stream_smem_bytes(variant, mb, kind == 2 ? 1 : 0));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 cudaError_t stream_occupancy(int variant, int act, int mb, int* ctas_per_sm) {
-  // The chain instance must fit as many CTAs per SM (all of its CTAs are co-resident).
-  int one = 0, chain = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&one, stream_kernel(variant, act, mb, 0), kWarps * 32,
-                                                                stream_smem_bytes(variant, mb, 0));
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&chain, stream_kernel(variant, act, mb, 1), kWarps * 32,
-                                                    stream_smem_bytes(variant, mb, 0));
-  if (e != cudaSuccess) return e;
-  *ctas_per_sm = one < chain ? one : chain;
-  return cudaSuccess;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, stream_kernel(variant, act, mb, 0),
+                                                                kWarps * 32, stream_smem_bytes(variant, mb, 0));
+  return e;
 }
 
 namespace {
@@ -1035,28 +799,21 @@ cudaError_t encode_weights(int variant, const GemvArgs& a, CUtensorMap* tmw) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NOPS>
-cudaError_t fill_params(int variant, const GemvArgs* ops, int nops, uint32_t* gbar, StreamParams<NOPS>* p) {
+cudaError_t fill_params(int variant, const GemvArgs& a, StreamParams* p) {
   memset(p, 0, sizeof(*p));
-  for (int g = 0; g < nops; ++g) {
-    cudaError_t e = encode_weights(variant, ops[g], &p->op[g].tmw);
-    if (e != cudaSuccess) return e;
-    p->op[g].X = ops[g].X;
-    p->op[g].Y = ops[g].Y;
-    p->op[g].N = ops[g].N;
-    p->op[g].K = ops[g].K;
-    p->op[g].units = ops[g].units;
-    p->op[g].nspans = ops[g].nspans;
-    p->op[g].wact = ops[g].units < ops[g].wact ? ops[g].units : ops[g].wact;
-  }
-  p->ws = ops[0].ws;
-  p->cnt = ops[0].cnt;
-  p->err = ops[0].err;
-  p->gbar = gbar;
-  p->wact = 0;
-  for (int g = 0; g < nops; ++g) p->wact = ops[g].wact > p->wact ? ops[g].wact : p->wact;
-  p->nops = nops;
-  p->M = ops[0].M;
+  cudaError_t e = encode_weights(variant, a, &p->op.tmw);
+  if (e != cudaSuccess) return e;
+  p->op.X = a.X;
+  p->op.Y = a.Y;
+  p->op.N = a.N;
+  p->op.K = a.K;
+  p->op.units = a.units;
+  p->op.nspans = a.nspans;
+  p->op.wact = a.units < a.wact ? a.units : a.wact;
+  p->ws = a.ws;
+  p->cnt = a.cnt;
+  p->err = a.err;
+  p->M = a.M;
   return cudaSuccess;
 }
 
@@ -1065,8 +822,8 @@ cudaError_t fill_params(int variant, const GemvArgs* ops, int nops, uint32_t* gb
 cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas, cudaStream_t s) {
   if (!g_encode) return cudaErrorInitializationError;
   const int mb = stream_mb_for(a.M);
-  StreamParams<1> p;
-  cudaError_t e = fill_params(variant, &a, 1, nullptr, &p);
+  StreamParams p;
+  cudaError_t e = fill_params(variant, a, &p);
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the kernel may start (and stream weights)
   // while the previous kernel on the stream drains; it calls
@@ -1083,30 +840,7 @@ cudaError_t launch_gemv_stream(int variant, int act, const GemvArgs& a, int ctas
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, a.epi ? 2 : (deep ? 3 : 0)), args);
-}
-
-cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
-                              cudaStream_t s) {
-  if (!g_encode) return cudaErrorInitializationError;
-  if (nops < 1 || nops > kChainOps) return cudaErrorInvalidValue;
-  const int mb = stream_mb_for(ops[0].M);
-  static thread_local StreamParams<kChainOps> p;  // 9 KB: kept off the stack
-  cudaError_t e = fill_params(variant, ops, nops, gbar, &p);
-  if (e != cudaSuccess) return e;
-  // Cooperative: every CTA is resident at once, as the grid barriers need.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = stream_smem_bytes(variant, mb, 0);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, 1), args);
+  return cudaLaunchKernelExC(&cfg, stream_kernel(variant, act, mb, a.epi ? 1 : (deep ? 2 : 0)), args);
 }
 
 }  // namespace rocmfp4

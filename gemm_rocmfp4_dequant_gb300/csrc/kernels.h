@@ -44,12 +44,6 @@ int64_t stream_warps(int64_t tiles, int64_t nspans, int64_t unit_bytes, int64_t 
 // current device (noalloc.cu): 0 when it has not been set up there.  Reads
 // and clears them, and on a non-zero result zeroes its split counters.
 cudaError_t noalloc_error_bits(cudaStream_t s, uint32_t* bits);
-// Up to kChainOps products with the same variant, activation type, M and
-// wact, in order, in one cooperative launch with a grid barrier after each
-// product (gbar: a zeroed counter).
-constexpr int kChainOps = 48;
-cudaError_t launch_gemv_chain(int variant, int act, const GemvArgs* ops, int nops, uint32_t* gbar, int ctas,
-                              cudaStream_t s);
 
 // Tensor-core product Y[M][N] = X[M][K] . W[N][K]^T (tcgen05, decoded weights
 // in tensor memory).  Needs K % tc_k_multiple(variant) == 0, W and X 16-byte

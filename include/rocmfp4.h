@@ -177,14 +177,12 @@ typedef struct rocmfp4_gemv_op {
  * rocmfp4_gemm_ex for each in turn, and product i may read (through X)
  * memory that products 0 .. i-1 write.
  *
- * This is the decode-step form: for M <= 8, consecutive products whose K is
- * a multiple of 256 (dual) or 512 (single-scale) and whose W and X are
- * 16-byte aligned run in one cooperative launch of the streaming kernel per
- * group of up to 48, with a grid-wide barrier after each product.  Weights
- * never depend on earlier products, so the next product's weights stream
- * while the previous one finishes; its activations are read only after the
- * barrier.  Other products (and every product when M > 8) are launched one
- * by one.
+ * This is the decode-step form: one call for a list of products.  Each
+ * product is one launch, the launch rocmfp4_gemm_ex would make, in order on
+ * `stream`; streaming launches (M <= 8) are programmatic dependent launches,
+ * so a product's weights, which never depend on earlier products, stream
+ * while the previous product finishes, and its activations are read only
+ * once the previous launch has completed.
  *   - ops is host memory read during the call; count == 0 does nothing.
  *   - Y of a product must not overlap any W, nor the X or Y of another
  *     product of the chain, except that X of a later product may be (part
@@ -203,8 +201,8 @@ rocmfp4_status rocmfp4_gemv_chain(const rocmfp4_gemv_op *ops, int count, int64_t
  * caller maps its tensors to layouts.)
  *   - variants is host memory of `count` entries, read during the call.
  *   - The result is that of calling rocmfp4_gemm_ex for each product in turn
- *     with its own layout, bit for bit.  Consecutive products of one layout
- *     run as one single-layout chain; a change of layout starts another.
+ *     with its own layout, bit for bit: one launch per product, as in
+ *     rocmfp4_gemv_chain.
  *   - Every product is checked (shape, layout, pointers) before any launch;
  *     otherwise arguments, aliasing rules and errors as rocmfp4_gemv_chain. */
 rocmfp4_status rocmfp4_gemv_chain_mixed(const rocmfp4_gemv_op *ops, const rocmfp4_variant *variants,
