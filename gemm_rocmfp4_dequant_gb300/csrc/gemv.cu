@@ -61,10 +61,34 @@ constexpr size_t cta_red_bytes() {
 }
 
 
-// Per-warp ring stage: 32 weight rows x SPAN bytes, then the matching slice of
-// MB activation rows (MB >= M, rounded to 1, 2, 4 or 8), KU fp16/bf16 values each.
+// Per-warp ring stage.  MB = 1: 32 weight rows x SPAN bytes, then the unit's
+// KU activations.  MB >= 2 (M rounded up to 2, 4 or 8): first the unit's
+// slice of MB activation rows, KU fp16/bf16 values each, as one tensor copy
+// with the 128-byte swizzle (its 16-byte chunks XOR-permuted within each
+// 1024 bytes, so that the lanes' fragment loads hit distinct banks: without
+// it the eight rows of a load all fall in the same banks), then the weights;
+// the stage is a multiple of 1024 bytes, as the swizzle needs.
 template <int V, int MB>
-constexpr int stage_bytes() { return kTileRows * Fmt<V>::SPAN + MB * Fmt<V>::KU * 2; }
+constexpr int x_offset() { return MB == 1 ? kTileRows * Fmt<V>::SPAN : 0; }
+template <int V, int MB>
+constexpr int w_offset() { return MB == 1 ? 0 : MB * Fmt<V>::KU * 2; }
+template <int V, int MB>
+constexpr int stage_bytes() {
+  return MB == 1 ? kTileRows * Fmt<V>::SPAN + Fmt<V>::KU * 2
+                 : (MB * Fmt<V>::KU * 2 + kTileRows * Fmt<V>::SPAN + 1023) / 1024 * 1024;
+}
+// Slack for aligning the rings to 1024 bytes (MB >= 2).
+template <int MB>
+constexpr int ring_align_slack() { return MB == 1 ? 0 : 1024; }
+
+// Chunk k (16 bytes) of block `blk` (64 bytes of activations) of row q in a
+// swizzled activation slice: the logical offset's 16-byte chunk index XORed
+// with its 128-byte line index modulo 8.
+template <int V>
+RF4_DEV const uint4* x_chunk(const uint8_t* xs, int q, int blk, int k) {
+  const uint32_t off = (uint32_t)q * (Fmt<V>::KU * 2) + (uint32_t)blk * 64u + (uint32_t)k * 16u;
+  return reinterpret_cast<const uint4*>(xs + (off ^ (((off >> 7) & 7u) << 4)));
+}
 
 // Stages per warp: as many as fit in about 54 KB per CTA (four CTAs, 16 warps
 // per SM), at least 2 (one unit in flight while the previous one computes).
@@ -81,8 +105,8 @@ constexpr int kZeroBytes = 256;  // zero activations for lanes whose B column is
 
 template <int V, int MB, int DEEP = 0>
 constexpr size_t smem_bytes() {
-  return (size_t)kWarps * stages<V, MB, DEEP>() * stage_bytes<V, MB>() + (size_t)kWarps * stages<V, MB, DEEP>() * 8 +
-         cta_red_bytes<MB>() + kZeroBytes;
+  return (size_t)ring_align_slack<MB>() + (size_t)kWarps * stages<V, MB, DEEP>() * stage_bytes<V, MB>() +
+         (size_t)kWarps * stages<V, MB, DEEP>() * 8 + cta_red_bytes<MB>() + kZeroBytes;
 }
 
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t wact) {
@@ -145,28 +169,32 @@ __device__ __forceinline__ void issue_w(const CUtensorMap* tmw, int M, int t, in
                                         int lane) {
   using F = Fmt<V>;
   if (lane == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)(kTileRows * F::SPAN + M * F::KU * 2));
+    // MB >= 2: the activation box has MB rows (rows past M arrive as zeros)
+    mbar_arrive_expect_tx(bar, (uint32_t)(kTileRows * F::SPAN + (MB == 1 ? M : MB) * F::KU * 2));
+    uint8_t* dst = stage + w_offset<V, MB>();
     if constexpr (EPI)  // box {span, 16 rows, gate and up halves}: gate rows land in rows 0-15, up rows in 16-31
-      tma_load_3d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * (kTileRows / 2), 0, bar);
+      tma_load_3d(smem_addr(dst), tmw, j * (F::SPAN / 4), t * (kTileRows / 2), 0, bar);
     else
-      tma_load_2d(smem_addr(stage), tmw, j * (F::SPAN / 4), t * kTileRows, bar);
+      tma_load_2d(smem_addr(dst), tmw, j * (F::SPAN / 4), t * kTileRows, bar);
   }
 }
 
 template <int V, int MB>
-__device__ __forceinline__ void issue_x(const uint16_t* __restrict__ X, int64_t K, int M, int j, uint8_t* stage,
+__device__ __forceinline__ void issue_x(const uint16_t* __restrict__ X, const CUtensorMap* tmx, int j, uint8_t* stage,
                                         uint32_t bar, int lane) {
   using F = Fmt<V>;
-  constexpr int XROW = F::KU * 2;
-  if (lane < M)
-    bulk_g2s(smem_addr(stage + kTileRows * F::SPAN + lane * XROW), X + (int64_t)lane * K + (int64_t)j * F::KU, XROW,
-             bar);
+  if (lane != 0) return;
+  if constexpr (MB == 1)
+    bulk_g2s(smem_addr(stage + x_offset<V, MB>()), X + (int64_t)j * F::KU, F::KU * 2, bar);
+  else  // box {64 values, KU / 64 lines, MB rows} at line j * KU / 64, swizzled
+    tma_load_3d(smem_addr(stage + x_offset<V, MB>()), tmx, 0, j * (F::KU / 64), 0, bar);
 }
 
 // One product of a launch.  The tensor map views the weights as N rows of
 // row_bytes / 4 32-bit words, with a box of SPAN / 4 words x 32 rows.
 struct StreamOp {
   CUtensorMap tmw;
+  CUtensorMap tmx;  // activations as {64 values, K / 64 lines, M rows}, 128-byte swizzle (M >= 2)
   const uint16_t* X;
   float* Y;
   int64_t N, K, units, nspans;
@@ -189,9 +217,8 @@ template <int V, int ACT, int MB>
 RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2][4], const uint4* zero) {
   using F = Fmt<V>;
   constexpr int SW = F::SW;
-  constexpr int XROW = F::KU * 2;
   const int q = lane >> 2, c = lane & 3;
-  const uint8_t* sb = stage + c * F::LANE_BYTES;
+  const uint8_t* sb = stage + w_offset<V, MB>() + c * F::LANE_BYTES;
   // rows q, q+8 (m-tile 0) and q+16, q+24 (m-tile 1): words of the lane span,
   // loaded inside each block's step (only that block's words stay live)
   auto load_words = [&](uint32_t (&w0)[SW], uint32_t (&w1)[SW], uint32_t (&w2)[SW], uint32_t (&w3)[SW]) {
@@ -214,7 +241,7 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
     const uint32_t sel0 = !bact ? 0x4444u : (hb ? 0x1044u : 0x4410u);  // (x[2s], 0) or (0, x[2s+16])
     const uint32_t sel1 = !bact ? 0x4444u : (hb ? 0x3244u : 0x4432u);  // (x[2s+1], 0) or (0, x[2s+17])
     // the 16 activations of half hb of block c*BPL + phi at xp[phi * 4 + 0..1]
-    const uint4* xp = bact ? reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN) + c * F::BPL * 4 + 2 * hb
+    const uint4* xp = bact ? reinterpret_cast<const uint4*>(stage + x_offset<V, MB>()) + c * F::BPL * 4 + 2 * hb
                            : zero;
 #pragma unroll
     for (int phi = 0; phi < F::BPL; ++phi) {
@@ -265,8 +292,8 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
     // D accumulates the whole unit (2 dual or 4 single-scale blocks = 16 or
     // 32 MMAs) and is then flushed into round-to-nearest fp32 registers.
     // Lane (q, c) holds B column q: activation row q, or zeros for q >= M.
-    const uint4* xp = q < M ? reinterpret_cast<const uint4*>(stage + kTileRows * F::SPAN + q * XROW) + c * F::BPL * 4
-                            : zero;
+    const uint8_t* xs = stage + x_offset<V, MB>();
+    const bool xrow = q < M;
     float d0[4], d1[4];
 #pragma unroll
     for (int phi = 0; phi < F::BPL; ++phi) {
@@ -276,7 +303,7 @@ RF4_DEV void compute_unit(const uint8_t* stage, int lane, int M, float (&acc)[2]
       uint32_t xv[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint4 v = xp[phi * 4 + k];
+        const uint4 v = xrow ? *x_chunk<V>(xs, q, c * F::BPL + phi, k) : zero[phi * 4 + k];
         xv[4 * k] = v.x;
         xv[4 * k + 1] = v.y;
         xv[4 * k + 2] = v.z;
@@ -595,14 +622,16 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
   const int warp = threadIdx.x >> 5;
   const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;
 
-  uint8_t* ring = smem + (size_t)warp * NS * SB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * NS * SB) + warp * NS;
+  // the rings start on a 1024-byte boundary when the activations are swizzled
+  uint8_t* const base = smem + (ring_align_slack<MB>() ? (1024u - (smem_addr(smem) & 1023u)) & 1023u : 0u);
+  uint8_t* ring = base + (size_t)warp * NS * SB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)kWarps * NS * SB) + warp * NS;
   // after every warp's stage barriers: the shared part of the split-tile
   // reduction, then a page of zeros
   CtaRed red;
-  red.rec = reinterpret_cast<float*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
+  red.rec = reinterpret_cast<float*>(base + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8);
   red.cnt = reinterpret_cast<uint32_t*>(red.rec + kWarps * 2 * kTileRows * MB);  // used only if cta_red_bytes<MB>() > 0
-  uint4* zero = reinterpret_cast<uint4*>(smem + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + cta_red_bytes<MB>());
+  uint4* zero = reinterpret_cast<uint4*>(base + (size_t)kWarps * NS * SB + (size_t)kWarps * NS * 8 + cta_red_bytes<MB>());
   if (threadIdx.x < kZeroBytes / 16) zero[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   if (cta_red_bytes<MB>() > 0 && threadIdx.x < kWarps) red.cnt[threadIdx.x] = 0u;
   __syncthreads();  // every thread of the CTA gets here: inactive warps return below
@@ -632,7 +661,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) gemv_stream_kernel(const __gri
     ++iw;
   };
   auto issue_x1 = [&]() {
-    issue_x<V, MB>(op.X, op.K, M, jx, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
+    issue_x<V, MB>(op.X, &op.tmx, jx, ring + (size_t)sx * SB, smem_addr(&bars[sx]), lane);
     if (++jx == S) jx = 0;
     if (++sx == NS) sx = 0;
     ++ix;
@@ -799,10 +828,26 @@ cudaError_t encode_weights(int variant, const GemvArgs& a, CUtensorMap* tmw) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Activations of M >= 2 rows as {64 values, K / 64 lines of 128 bytes, M
+// rows}; a box is one unit's slice of MB rows, with the 128-byte swizzle.
+cudaError_t encode_acts(int variant, const GemvArgs& a, int mb, CUtensorMap* tmx) {
+  const int ku = variant == 0 ? Fmt<0>::KU : Fmt<1>::KU;
+  cuuint64_t dims[3] = {64, (cuuint64_t)(a.K / 64), (cuuint64_t)a.M};
+  cuuint64_t strides[2] = {128, (cuuint64_t)a.K * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)(ku / 64), (cuuint32_t)mb};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(tmx, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(a.X), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t fill_params(int variant, const GemvArgs& a, StreamParams* p) {
   memset(p, 0, sizeof(*p));
   cudaError_t e = encode_weights(variant, a, &p->op.tmw);
   if (e != cudaSuccess) return e;
+  const int mb = stream_mb_for(a.M);
+  if (mb >= 2 && (e = encode_acts(variant, a, mb, &p->op.tmx)) != cudaSuccess) return e;
   p->op.X = a.X;
   p->op.Y = a.Y;
   p->op.N = a.N;
