@@ -133,18 +133,41 @@ RF4_DEV float ue4m3_f32(uint32_t e) {
   return E ? __uint_as_float(((E + 120u) << 23) | (M << 20)) : (float)M * (1.0f / 512.0f);
 }
 
+// The scale byte of a group: E4M3 values increase with the byte, so this is
+// the smallest e with 5 * E4M3(e) >= amax.  A candidate comes from the fp32
+// bits of amax * 0.2 (E4M3 rounded up: within one step of the answer, as the
+// estimate is within a few ulp of amax / 5); one exact check each way (5 *
+// E4M3(e) is exact in fp32) then fixes it.
 RF4_DEV uint32_t quant_scale(float amax) {
   if (!(amax > 0.f)) return 0u;
   if (5.f * ue4m3_f32(0x7Eu) < amax) return 0x7Eu;
-  uint32_t lo = 0, hi = 0x7E;  // E4M3 values increase with the byte: 7 halvings of [0, 0x7E]
-#pragma unroll
-  for (int it = 0; it < 7; ++it) {
-    const uint32_t mid = (lo + hi) >> 1;
-    const bool cover = 5.f * ue4m3_f32(mid) >= amax;
-    hi = cover ? mid : hi;
-    lo = cover ? lo : mid + 1;
+  const float t = amax * 0.2f;
+  uint32_t e;
+  if (t >= 0.015625f) {  // 2^-6 and up: E4M3 exponent field E >= 1
+    const uint32_t b = __float_as_uint(t);
+    uint32_t E = (b >> 23) - 120u, M = (b >> 20) & 7u;
+    if (b & 0xFFFFFu) ++M;  // round the 3-bit mantissa up
+    if (M == 8u) {
+      M = 0u;
+      ++E;
+    }
+    e = E > 15u ? 0x7Eu : (E << 3) | M;
+  } else {  // subnormal E4M3: value M / 512
+    e = (uint32_t)ceilf(t * 512.f);  // at most 8, which is 2^-6 (E = 1, M = 0)
   }
-  return lo;
+  e = e > 0x7Eu ? 0x7Eu : (e == 0u ? 1u : e);
+  if (e > 1u && 5.f * ue4m3_f32(e - 1u) >= amax) --e;
+  else if (5.f * ue4m3_f32(e) < amax) ++e;
+  return e;
+}
+
+// The Codebook10 midpoints 0.5, 1.5, 2.5, 3.5, 5, 7, 9 as fp16 (ACT = 0) or
+// bf16 bits, in both lanes.
+template <int ACT>
+RF4_HOSTDEV constexpr uint32_t mid_pair(int j) {
+  constexpr uint32_t f16[7] = {0x3800u, 0x3E00u, 0x4100u, 0x4300u, 0x4500u, 0x4700u, 0x4880u};
+  constexpr uint32_t bf16[7] = {0x3F00u, 0x3FC0u, 0x4020u, 0x4060u, 0x40A0u, 0x40E0u, 0x4110u};
+  return ACT == 0 ? f16[j] | (f16[j] << 16) : bf16[j] | (bf16[j] << 16);
 }
 
 // Packed source pairs.  Every threshold of the rule, a Codebook10 midpoint
@@ -152,7 +175,8 @@ RF4_DEV uint32_t quant_scale(float amax) {
 // bits, 2^-10 .. 224), has at most 8 significant bits and lies in
 // [2^-11, 2016]: it is exact in fp16 and in bf16, so comparing a source value
 // with it in the source's own 16-bit format is the exact comparison.  Two
-// values are compared per instruction.
+// values are compared per instruction, and the thresholds themselves are
+// packed products (exact).
 template <int ACT>
 struct Pack {
   // |x| per lane with non-finite lanes set to 0 (they count as 0)
@@ -169,26 +193,30 @@ struct Pack {
   static RF4_DEV uint32_t broadcast(float f) {
     uint32_t h;
     if constexpr (ACT == 0)
-      h = __half_as_ushort(__float2half_rn(f));
+      asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(h) : "f"(f));
     else
-      h = __float_as_uint(f) >> 16;
-    return h | (h << 16);
+      asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(h) : "f"(f));
+    return h;
   }
-  // per lane: 1 if a > t (a clean, t a threshold), summed onto c
-  static RF4_DEV uint32_t count_gt(uint32_t c, uint32_t a, uint32_t t) {
-    uint32_t g;
-    if constexpr (ACT == 0) {
-      asm("set.gt.f16x2.f16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
-      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(c), "r"(g));
-    } else {
-      asm("set.gt.bf16x2.bf16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
-      asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(c), "r"(g));
+  // the thresholds mid[j] * hs of a half-scale pair hs2 (exact products)
+  static RF4_DEV void thresholds(uint32_t hs2, uint32_t (&t)[7]) {
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      if constexpr (ACT == 0)
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t[j]) : "r"(hs2), "r"(mid_pair<ACT>(j)));
+      else
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t[j]) : "r"(hs2), "r"(mid_pair<ACT>(j)));
     }
-    return c;
   }
-  // counts start at 1024 (fp16) / 128 (bf16), where the format's unit in the
-  // last place is 1, so a count k <= 7 sits in the low 3 bits of each lane
-  static constexpr uint32_t kCountBase = ACT == 0 ? 0x64006400u : 0x43004300u;
+  // per lane: 0xFFFF if a > t, else 0
+  static RF4_DEV uint32_t gt_mask(uint32_t a, uint32_t t) {
+    uint32_t g;
+    if constexpr (ACT == 0)
+      asm("set.gt.u32.f16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
+    else
+      asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(g) : "r"(a), "r"(t));
+    return g;
+  }
   static RF4_DEV float to_f32(uint32_t h) {
     if constexpr (ACT == 0)
       return __half2float(__ushort_as_half((uint16_t)h));
@@ -203,23 +231,59 @@ struct Pack {
 // high lane in bits 16-19.
 template <int ACT>
 RF4_DEV uint32_t pair_codes(uint32_t w, uint32_t a, const uint32_t (&t)[7]) {
-  uint32_t c = Pack<ACT>::kCountBase;
-#pragma unroll
-  for (int j = 0; j < 7; ++j) c = Pack<ACT>::count_gt(c, a, t[j]);
-  const uint32_t k = c & 0x00070007u;
+  // k = #{j : a > t[j]} per lane by binary search over the increasing
+  // thresholds: a > t[3] iff k >= 4, then t[5] or t[1], then one of t[6],
+  // t[4], t[2], t[0]; the per-lane masks select the next threshold.
+  const uint32_t g1 = Pack<ACT>::gt_mask(a, t[3]);
+  const uint32_t g2 = Pack<ACT>::gt_mask(a, (g1 & t[5]) | (~g1 & t[1]));
+  const uint32_t hi = (g1 & t[6]) | (~g1 & t[2]), lo = (g1 & t[4]) | (~g1 & t[0]);
+  const uint32_t g3 = Pack<ACT>::gt_mask(a, (g2 & hi) | (~g2 & lo));
+  const uint32_t k = (g1 & 0x00040004u) | (g2 & 0x00020002u) | (g3 & 0x00010001u);
   // sign bit 15 / 31 to bit 3 / 19 of the lanes with a nonzero count
   const uint32_t nz = (k + 0x00070007u) & 0x00080008u;  // bit 3 of a lane set iff its k != 0
   return k | ((w >> 12) & nz);
 }
 
+constexpr int kQuantThreads = 128;
+
 template <int V, int ACT>
-__global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __restrict__ W, int64_t nblocks, bool vec) {
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const uint16_t* __restrict__ src,
+                                                                   uint8_t* __restrict__ W, int64_t nblocks, bool vec,
+                                                                   bool wvec) {
   using F = Fmt<V>;
-  for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks;
+  // Per warp: its 32 source blocks staged by coalesced 16-byte loads (64
+  // bytes each, 16 bytes of padding after each so the per-block reads hit
+  // distinct banks), and its 32 output blocks (contiguous, 18 or 17 bytes
+  // each) staged for coalesced 16-byte stores.
+  __shared__ __align__(16) uint8_t in_stage[kQuantThreads / 32][32 * 80];
+  __shared__ __align__(16) uint8_t out_stage[kQuantThreads / 32][32 * 18];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk - lane < nblocks;
        blk += (int64_t)gridDim.x * blockDim.x) {
+    // the warp's 32 blocks are all in range (a warp-uniform test)
+    const bool full = blk - lane + 32 <= nblocks;
     uint32_t w[16];  // w[i] = (value 2i, value 2i+1)
     const uint16_t* s = src + blk * 32;
-    if (vec) {
+    if (vec && full) {
+      const uint4* g = reinterpret_cast<const uint4*>(src + (blk - lane) * 32);
+      __syncwarp();  // the previous step's reads of the stage are done
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ci = q * 32 + lane;  // chunk ci of the warp's 2 KB: block ci / 4, part ci % 4
+        *reinterpret_cast<uint4*>(&in_stage[wib][(ci >> 2) * 80 + (ci & 3) * 16]) = g[ci];
+      }
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(&in_stage[wib][lane * 80 + q * 16]);
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+      }
+    } else if (blk >= nblocks) {
+      continue;  // a lane past the end of a partial warp
+    } else if (vec) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 v = reinterpret_cast<const uint4*>(s)[q];
@@ -234,15 +298,14 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
     }
     // value i: w[i / 2] half i % 2; scale group 0 = values 0..15, group 1 = 16..31 (dual)
     uint32_t a[16];
-    uint32_t m0 = 0, m1 = 0;  // largest |value| bits per group: non-negative values order as their bits
+    uint32_t m0 = 0, m1 = 0;  // largest |value| bits per group and lane: non-negative values order as their bits
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       a[i] = Pack<ACT>::clean_abs(w[i]);
-      const uint32_t hi = max(a[i] & 0xFFFFu, a[i] >> 16);
-      if (i < 8) m0 = max(m0, hi);
-      else m1 = max(m1, hi);
+      if (i < 8) m0 = __vmaxu2(m0, a[i]);
+      else m1 = __vmaxu2(m1, a[i]);
     }
-    const float am0 = Pack<ACT>::to_f32(m0), am1 = Pack<ACT>::to_f32(m1);
+    const float am0 = Pack<ACT>::to_f32(max(m0 & 0xFFFFu, m0 >> 16)), am1 = Pack<ACT>::to_f32(max(m1 & 0xFFFFu, m1 >> 16));
     uint32_t e0, e1;
     if constexpr (V == 0) {
       e0 = quant_scale(am0);
@@ -253,13 +316,9 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
     const float hs0 = 0.5f * ue4m3_f32(e0), hs1 = 0.5f * ue4m3_f32(e1);
     // thresholds: midpoints of the magnitudes {0,1,2,3,4,6,8,10} times the half-scale
     // (a zero half-scale gives zero thresholds, and a group of zeros gives codes 0)
-    const float mid[7] = {0.5f, 1.5f, 2.5f, 3.5f, 5.f, 7.f, 9.f};
     uint32_t t0[7], t1[7];
-#pragma unroll
-    for (int j = 0; j < 7; ++j) {
-      t0[j] = Pack<ACT>::broadcast(mid[j] * hs0);
-      t1[j] = Pack<ACT>::broadcast(mid[j] * hs1);
-    }
+    Pack<ACT>::thresholds(Pack<ACT>::broadcast(hs0), t0);
+    Pack<ACT>::thresholds(Pack<ACT>::broadcast(hs1), t1);
     // byte j: value j (low nibble, group 0) and value j + 16 (high nibble, group 1);
     // o16[i] = bytes 2i and 2i+1 = codes of values 2i, 2i+16, 2i+1, 2i+17
     uint32_t o16[8];
@@ -268,7 +327,9 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
       const uint32_t cl = pair_codes<ACT>(w[i], a[i], t0), ch = pair_codes<ACT>(w[8 + i], a[8 + i], t1);
       o16[i] = (cl & 0xFu) | ((ch & 0xFu) << 4) | ((cl >> 16) << 8) | ((ch >> 16) << 12);
     }
-    uint8_t* out = W + blk * F::BB;
+    const bool coop = wvec && full;  // the warp's output (32 blocks, a multiple of 16 bytes) is 16-byte aligned
+    uint8_t* out = coop ? &out_stage[wib][lane * F::BB] : W + blk * F::BB;
+    if (coop) __syncwarp();  // the previous step's reads of the output stage are done
     if constexpr (V == 0) {  // 18-byte blocks start on even addresses: nine 16-bit stores
       uint16_t* p16 = reinterpret_cast<uint16_t*>(out);
 #pragma unroll
@@ -281,6 +342,14 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ src, uint8_t* __res
         out[2 * k + 1] = (uint8_t)(o16[k] >> 8);
       }
       out[16] = (uint8_t)e0;
+    }
+    if (coop) {
+      __syncwarp();
+      constexpr int kChunks = 32 * F::BB / 16;  // 36 or 34
+      uint4* g = reinterpret_cast<uint4*>(W + (blk - lane) * F::BB);
+      const uint4* st = reinterpret_cast<const uint4*>(out_stage[wib]);
+      g[lane] = st[lane];
+      if (lane < kChunks - 32) g[32 + lane] = st[32 + lane];
     }
   }
 }
@@ -324,13 +393,14 @@ cudaError_t launch_validate(int variant, const uint8_t* W, int64_t nblocks, unsi
 cudaError_t launch_quantize(int variant, int act, const uint16_t* src, uint8_t* W, int64_t nblocks, cudaStream_t s) {
   if (nblocks == 0) return cudaSuccess;
   const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-  const int threads = 128, grid = grid_for(nblocks, threads);
+  const bool wvec = (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+  const int threads = kQuantThreads, grid = grid_for(nblocks, threads);
   if (variant == 0) {
-    if (act == 0) quantize_kernel<0, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
-    else quantize_kernel<0, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+    if (act == 0) quantize_kernel<0, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec, wvec);
+    else quantize_kernel<0, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec, wvec);
   } else {
-    if (act == 0) quantize_kernel<1, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
-    else quantize_kernel<1, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec);
+    if (act == 0) quantize_kernel<1, 0><<<grid, threads, 0, s>>>(src, W, nblocks, vec, wvec);
+    else quantize_kernel<1, 1><<<grid, threads, 0, s>>>(src, W, nblocks, vec, wvec);
   }
   return cudaGetLastError();
 }
