@@ -539,11 +539,13 @@ def per_matrix_kernel_times(L: GemvStep, reps=None, ceilings=None):
     return out
 
 
-def e2e_rate(L: GemvStep, steps, warmup, world):
+def e2e_rate(L: GemvStep, steps, warmup, world, staged=True):
     """The metric through the public API with host buffers: every step copies the
     step's activations (all matrices', packed in one pinned host buffer) to the
     device, runs the products through the API and reads all outputs back into one
-    pinned host buffer; weights stay resident."""
+    pinned host buffer; weights stay resident.  staged: both transfers by the
+    library's staging copy (rocmfp4_copy, a kernel in the chain of dependent
+    launches); else by torch copies on the copy engines."""
     import torch
     xs = [x.numel() for x in L.X[0]]
     ys = [y.numel() for y in L.Y[0]]
@@ -558,10 +560,16 @@ def e2e_rate(L: GemvStep, steps, warmup, world):
 
     def one(i):
         r = i % L.copies
-        dx_all.copy_(hx[r], non_blocking=True)
+        if staged:
+            L.rf4.copy(dx_all, hx[r])
+        else:
+            dx_all.copy_(hx[r], non_blocking=True)
         for m, (name, N, K) in enumerate(L.mats):
             L.rf4.gemm(L.W[r][m], dx[m], N, K, L.variant, Y=dy[m])
-        hy[r].copy_(dy_all, non_blocking=True)
+        if staged:
+            L.rf4.copy(hy[r], dy_all)
+        else:
+            hy[r].copy_(dy_all, non_blocking=True)
 
     t = time_steps(one, steps, warmup, world)
     return t, h2d, d2h
@@ -596,8 +604,13 @@ def run_gemv(args, world, hbm, mats, variant=0, M=1, act=0, with_e2e=True, with_
         ne = max(10, args.steps // 4)
         te, h2d, d2h = e2e_rate(L, ne, args.warmup, world)
         te = max_over_ranks(te, world)
+        tc, _, _ = e2e_rate(L, ne, args.warmup, world, staged=False)
+        tc = max_over_ranks(tc, world)
         res["e2e"] = {"value": round(world * sb * ne / te / 1e9, 1), "unit": "GB/s",
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "transfers": "rocmfp4_copy (staging kernel in the chain of dependent launches) from and to "
+                                   "pinned host buffers, every step",
+                      "copy_engine_GB/s": round(world * sb * ne / tc / 1e9, 1)}
     del L
     torch.cuda.empty_cache()
     return res

@@ -25,7 +25,7 @@ STATUS = {0: "ROCMFP4_OK", 1: "ROCMFP4_ERR_INVALID_ARG", 2: "ROCMFP4_ERR_UNSUPPO
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librocmfp4.so")
 EXPORTS = ("rocmfp4_block_bytes", "rocmfp4_row_bytes", "rocmfp4_gemv", "rocmfp4_gemv_ex", "rocmfp4_gemm",
-           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_quantize", "rocmfp4_gemv_chain", "rocmfp4_gemv_chain_mixed", "rocmfp4_dequant", "rocmfp4_validate", "rocmfp4_device_error_bits",
+           "rocmfp4_gemm_ex", "rocmfp4_gemm_noalloc", "rocmfp4_gemv_gate_up", "rocmfp4_decode_attention", "rocmfp4_quantize", "rocmfp4_gemv_chain", "rocmfp4_gemv_chain_mixed", "rocmfp4_dequant", "rocmfp4_copy", "rocmfp4_validate", "rocmfp4_device_error_bits",
            "rocmfp4_status_string", "rocmfp4_last_error", "rocmfp4_launch_count", "rocmfp4_shutdown")
 
 _lib = None
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "rocmfp4_gemv_chain": ([ctypes.POINTER(GemvOp), c_int, i64, c_int, c_int, vp], c_int),
         "rocmfp4_gemv_chain_mixed": ([ctypes.POINTER(GemvOp), ctypes.POINTER(c_int), c_int, i64, c_int, vp], c_int),
         "rocmfp4_dequant": ([vp, vp, c_int, i64, i64, c_int, vp], c_int),
+        "rocmfp4_copy": ([vp, vp, i64, vp], c_int),
         "rocmfp4_validate": ([vp, i64, i64, c_int, ctypes.POINTER(i64), vp], c_int),
         "rocmfp4_device_error_bits": ([vp], u32),
         "rocmfp4_status_string": ([c_int], ctypes.c_char_p),
@@ -265,6 +266,23 @@ def gemv_chain(ops, variant=DUAL, stream=None):
         _check(load().rocmfp4_gemv_chain_mixed(arr, varr, len(ops), M, act, _stream(stream)), "rocmfp4_gemv_chain_mixed")
     else:
         _check(load().rocmfp4_gemv_chain(arr, len(ops), M, variant, act, _stream(stream)), "rocmfp4_gemv_chain")
+
+
+def copy(dst, src, stream=None):
+    """Copies src into dst (the same number of bytes) on the stream by a kernel
+    (rocmfp4_copy): each is a contiguous CUDA tensor or a pinned CPU tensor.  It
+    runs after the stream's preceding kernel and lets the next one begin early."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src must hold the same number of bytes")
+    if nbytes == 0:
+        return
+    _check(load().rocmfp4_copy(dst.data_ptr(), src.data_ptr(), nbytes, _stream(stream)), "rocmfp4_copy")
 
 
 def quantize(src, variant: int = DUAL, W=None, stream=None):

@@ -444,6 +444,33 @@ rocmfp4_status rocmfp4_quantize(const void* src, rocmfp4_act src_type, void* W, 
   return ROCMFP4_OK;
 }
 
+rocmfp4_status rocmfp4_copy(void* dst, const void* src, int64_t bytes, rocmfp4_stream_t stream) {
+  if (bytes < 0) return fail(ROCMFP4_ERR_INVALID_ARG, "negative size");
+  if (bytes == 0) return ROCMFP4_OK;
+  if (dst == nullptr || src == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "NULL pointer");
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dst), sp = reinterpret_cast<uintptr_t>(src);
+  if ((d < sp ? sp - d : d - sp) < (uintptr_t)bytes) return fail(ROCMFP4_ERR_INVALID_ARG, "overlapping ranges");
+  // Each side must be memory a kernel can address: device or managed memory,
+  // or pinned host memory (through its device pointer).  Pageable host memory
+  // is refused rather than handed to the kernel.
+  void* ends[2] = {dst, const_cast<void*>(src)};
+  for (void*& p : ends) {
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (at.type == cudaMemoryTypeUnregistered)
+      return fail(ROCMFP4_ERR_INVALID_ARG, "pageable host memory: pin it (cudaHostAlloc / cudaHostRegister)");
+    if (at.type == cudaMemoryTypeHost) {
+      if (at.devicePointer == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "host memory not mapped for the device");
+      p = at.devicePointer;
+    }
+  }
+  cudaError_t e = launch_copy(ends[0], ends[1], bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy launch");
+  g_launches.fetch_add(1);
+  return ROCMFP4_OK;
+}
+
 rocmfp4_status rocmfp4_validate(const void* W, int64_t N, int64_t K, rocmfp4_variant variant,
                                 int64_t* first_bad_block, rocmfp4_stream_t stream) {
   if (first_bad_block) *first_bad_block = -1;

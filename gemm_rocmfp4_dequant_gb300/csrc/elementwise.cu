@@ -1,6 +1,8 @@
 // Elementwise ROCmFP4 kernels: dequantisation, scale validation, the
-// quantiser (fp16 / bf16 -> ROCmFP4 blocks), and the generic product used
-// when a shape or pointer alignment does not fit the streaming kernel.
+// quantiser (fp16 / bf16 -> ROCmFP4 blocks), the generic product used
+// when a shape or pointer alignment does not fit the streaming kernel, and
+// the staging copy that moves a decode step's inputs and outputs between
+// pinned host memory and the device inside a chain of dependent launches.
 // Decode follows "Feasibility Report: Porting ROCmFP4 to Atlas", section
 // "What is ROCmFP4?" (Block Layout, Codebook10 Value Table, Scale Format), in
 // plain fp32 arithmetic that is exact for every weight; the quantiser inverts
@@ -354,6 +356,30 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const uint16_t*
   }
 }
 
+// ---- staging copy (host <-> device, either side pinned host or device) -------------
+// Launched with programmatic dependent launch: the next kernel on the stream
+// may begin launching at once (a following product's weights then stream
+// while this copy runs), and nothing is read or written before the preceding
+// kernel has completed.  One 16-byte vector per thread when both pointers are
+// 16-byte aligned (the tail and unaligned copies go byte by byte).
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_kernel(uint8_t* __restrict__ dst,
+                                                             const uint8_t* __restrict__ src, int64_t bytes,
+                                                             bool vec) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int64_t tid = (int64_t)blockIdx.x * kCopyThreads + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * kCopyThreads;
+  int64_t done = 0;
+  if (vec) {
+    const int64_t n16 = bytes >> 4;
+    for (int64_t i = tid; i < n16; i += nth) reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    done = n16 << 4;
+  }
+  for (int64_t i = done + tid; i < bytes; i += nth) dst[i] = src[i];
+}
+
 int grid_for(int64_t work, int threads) {
   int64_t g = (work + threads - 1) / threads;
   if (g > 152 * 32) g = 152 * 32;
@@ -412,6 +438,22 @@ cudaError_t launch_gemm_generic(int variant, int act, const GenericArgs& a, cuda
   if (variant == 0) gemm_generic_kernel<0><<<(unsigned)grid, warps * 32, 0, s>>>(a, act);
   else gemm_generic_kernel<1><<<(unsigned)grid, warps * 32, 0, s>>>(a, act);
   return cudaGetLastError();
+}
+
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s) {
+  if (bytes <= 0) return cudaSuccess;
+  const bool vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_for(vec ? (bytes + 15) / 16 : bytes, kCopyThreads));
+  cfg.blockDim = dim3(kCopyThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, copy_kernel, static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src), bytes,
+                            vec);
 }
 
 }  // namespace rocmfp4

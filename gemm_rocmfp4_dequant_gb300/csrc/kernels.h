@@ -104,4 +104,8 @@ cudaError_t launch_quantize(int variant, int act, const uint16_t* src, uint8_t* 
 cudaError_t launch_validate(int variant, const uint8_t* W, int64_t nblocks, unsigned long long* first,
                             cudaStream_t s);
 
+// Stream-ordered copy of `bytes` bytes by a kernel (programmatic dependent
+// launch); each pointer is device memory or device-addressable host memory.
+cudaError_t launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t s);
+
 }  // namespace rocmfp4

@@ -74,6 +74,13 @@ def test_host_argument_checks_return_invalid_arg(L):
     assert L.rocmfp4_dequant(fake, fake, 7, 4, 32, 0, ok_stream) == 1
     assert L.rocmfp4_validate(fake, 4, 40, 0, None, ok_stream) == 1
     assert b"multiple of 32" in L.rocmfp4_last_error() or L.rocmfp4_last_error() != b""
+    # staging copy: negative size, NULL pointers, overlapping ranges
+    assert L.rocmfp4_copy(fake, _vp(0x9000), -1, ok_stream) == 1
+    assert L.rocmfp4_copy(null, fake, 16, ok_stream) == 1
+    assert L.rocmfp4_copy(fake, null, 16, ok_stream) == 1
+    assert L.rocmfp4_copy(_vp(0x1000), _vp(0x1008), 16, ok_stream) == 1
+    assert L.rocmfp4_copy(_vp(0x1008), _vp(0x1000), 16, ok_stream) == 1
+    assert b"overlapping" in L.rocmfp4_last_error()
 
 
 def test_empty_shapes_are_no_ops(L):
@@ -81,5 +88,6 @@ def test_empty_shapes_are_no_ops(L):
     assert L.rocmfp4_gemm(null, null, null, 0, 8, 64, 0) == 0
     assert L.rocmfp4_gemm(null, null, null, 3, 0, 64, 0) == 0
     assert L.rocmfp4_dequant(null, null, 0, 0, 64, 1, null) == 0
+    assert L.rocmfp4_copy(null, null, 0, null) == 0
     first = ctypes.c_int64(5)
     assert L.rocmfp4_validate(null, 0, 64, 0, ctypes.byref(first), null) == 0 and first.value == -1
