@@ -450,9 +450,13 @@ rocmfp4_status rocmfp4_copy(void* dst, const void* src, int64_t bytes, rocmfp4_s
   if (dst == nullptr || src == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "NULL pointer");
   const uintptr_t d = reinterpret_cast<uintptr_t>(dst), sp = reinterpret_cast<uintptr_t>(src);
   if ((d < sp ? sp - d : d - sp) < (uintptr_t)bytes) return fail(ROCMFP4_ERR_INVALID_ARG, "overlapping ranges");
-  // Each side must be memory a kernel can address: device or managed memory,
-  // or pinned host memory (through its device pointer).  Pageable host memory
-  // is refused rather than handed to the kernel.
+  // Each side must be memory a kernel on the current device can address:
+  // its own device memory, managed memory, or pinned host memory (through
+  // its device pointer).  Pageable host memory and another device's memory
+  // are refused rather than handed to the kernel.
+  int cur = 0;
+  cudaError_t ce = cudaGetDevice(&cur);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
   void* ends[2] = {dst, const_cast<void*>(src)};
   for (void*& p : ends) {
     cudaPointerAttributes at{};
@@ -460,6 +464,8 @@ rocmfp4_status rocmfp4_copy(void* dst, const void* src, int64_t bytes, rocmfp4_s
     if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
     if (at.type == cudaMemoryTypeUnregistered)
       return fail(ROCMFP4_ERR_INVALID_ARG, "pageable host memory: pin it (cudaHostAlloc / cudaHostRegister)");
+    if (at.type == cudaMemoryTypeDevice && at.device != cur)
+      return fail(ROCMFP4_ERR_INVALID_ARG, "device memory of another device");
     if (at.type == cudaMemoryTypeHost) {
       if (at.devicePointer == nullptr) return fail(ROCMFP4_ERR_INVALID_ARG, "host memory not mapped for the device");
       p = at.devicePointer;

@@ -282,18 +282,20 @@ rocmfp4_status rocmfp4_validate(const void *W, int64_t N, int64_t K, rocmfp4_var
  * "Kernel System", the decode matvec): a step's activations come in from the
  * host and its results go back out without a copy-engine transfer that would
  * break the chain of dependent launches.
- *   - dst and src: device or managed memory, or pinned host memory
- *     (cudaHostAlloc, cudaMallocHost, cudaHostRegister), which the kernel
- *     reaches through its device pointer; pageable host memory is refused.
+ *   - dst and src: memory of the current device, managed memory, or pinned
+ *     host memory (cudaHostAlloc, cudaMallocHost, cudaHostRegister), which
+ *     the kernel reaches through its device pointer; pageable host memory
+ *     and another device's memory are refused.
  *     Both are owned by the caller; the ranges must not overlap.
  *   - The kernel is a programmatic dependent launch: the next kernel on the
  *     stream may begin launching at once (a following product's weights then
  *     stream while the copy runs), and the copy reads and writes nothing
  *     before the preceding kernel on the stream has completed.
  *   - 16-byte vectors when both pointers are 16-byte aligned, else bytes.
- * bytes == 0 is a no-op.  bytes < 0, a NULL pointer, overlapping ranges or
- * pageable host memory give ROCMFP4_ERR_INVALID_ARG; a failed pointer query
- * or launch gives ROCMFP4_ERR_CUDA.  Asynchronous on `stream`. */
+ * bytes == 0 is a no-op.  bytes < 0, a NULL pointer, overlapping ranges,
+ * pageable host memory or another device's memory give
+ * ROCMFP4_ERR_INVALID_ARG; a failed pointer query or launch gives
+ * ROCMFP4_ERR_CUDA.  Asynchronous on `stream`. */
 rocmfp4_status rocmfp4_copy(void *dst, const void *src, int64_t bytes, rocmfp4_stream_t stream);
 
 /* Error bits recorded by kernels on the current device since the last query
