@@ -127,3 +127,40 @@ def test_step_loop_with_staged_inputs_and_outputs(variant):
             yref = oracle.gemm(Wh[i], xb[xo:xo + K].reshape(1, K), N, K, variant, act=synth.ACT_F16)
             assert_close(got[s][o:o + N].reshape(1, N), yref, K, max_halfscale(Wh[i], variant), f"step {s} product {i}")
             o += N
+
+
+def test_step_captured_in_a_graph():
+    """The same step (copy in, product, copy out) captured once in a CUDA graph
+    and replayed with new host inputs: every replay sees its own inputs and
+    hands back its own outputs."""
+    t = torch()
+    N, K, variant = 1000, 1024, rf4.DUAL
+    Wh = synth.weights(N, K, variant, seed=9, stream=3200)
+    W = upload_w(Wh)
+    hx = t.empty(K, dtype=t.float16).pin_memory()
+    hy = t.full((N,), float("nan"), dtype=t.float32).pin_memory()
+    dx = t.empty((1, K), dtype=t.float16, device="cuda")
+    dy = t.empty((1, N), dtype=t.float32, device="cuda")
+
+    def step():
+        rf4.copy(dx, hx)
+        rf4.gemm(W, dx, N, K, variant, Y=dy)
+        rf4.copy(hy, dy)
+
+    s = t.cuda.Stream()
+    s.wait_stream(t.cuda.current_stream())
+    with t.cuda.stream(s):
+        step()  # the library's one-time set-up happens outside the capture
+    t.cuda.current_stream().wait_stream(s)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g):
+        step()
+    for rep in range(3):
+        bits = synth.activations(1, K, synth.ACT_F16, seed=200 + rep, stream=3300)
+        hx.copy_(t.from_numpy(bits.reshape(-1).view(np.int16)).view(t.float16))
+        hy.fill_(float("nan"))
+        g.replay()
+        t.cuda.synchronize()
+        yref = oracle.gemm(Wh, bits, N, K, variant, act=synth.ACT_F16)
+        assert_close(hy.numpy().reshape(1, N), yref, K, max_halfscale(Wh, variant), f"replay {rep}")
